@@ -1,0 +1,223 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the CPU oracle checks.
+
+This module only *draws* numbers and lays them out (shapes, bf16 rounding of
+the drawn values, paged block tables, NaN sentinels).  It contains none of the
+attention arithmetic: nothing here projects, rotates, scores or normalises.
+
+Workloads are shaped like the DeepSeek-V2 layer the pages describe
+("How does DeepSeek's Multi-Latent Attention (MLA) compress the KV cache below
+GQA?", zenaique, section "What MLA caches versus what MHA and GQA cache":
+latent width on the order of 512; "Multi-head Latent Attention" card,
+talentme, "Core Definition": d_c = 512), plus the tiny layer whose sizes
+match the numpy snippet of "What does Multi-head Latent Attention compress,
+and how is that different from quantizing the cache?" (katajob, "code").
+
+Recipe (all draws from ``numpy.random.default_rng``, PCG64):
+  * main stream, seeded with the workload seed, in this order:
+      W_DKV, W_KR, W_Q, W_QR, W_UK, W_UV, W_O   ~ N(0, 1/fan_in)
+      cached lengths (uniform integers, inclusive bounds)
+      x_ctx ~ N(0,1)       (only for workloads whose cache is built by append)
+      x_q   ~ N(0,1)       (hidden states of the new / query tokens)
+      block permutation
+  * latent rows for directly filled caches come from one sub-stream per
+    sequence (seed sequence [seed, 1000 + b]) so a single sequence can be
+    regenerated without drawing the whole cache.
+  * everything is drawn in float32; bf16 workloads round each value to bf16
+    (round to nearest even) before use, so the oracle sees exactly the values
+    the GPU stores.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK_SIZE = 64
+SPARE_BLOCKS = 8
+
+
+@dataclass(frozen=True)
+class Dims:
+    d_model: int
+    n_heads: int
+    qk_nope: int
+    d_rope: int
+    v_head: int
+    d_c: int
+    block_size: int = BLOCK_SIZE
+    rope_base: float = 10000.0
+
+    @property
+    def row(self) -> int:
+        """Elements in one cached row: latent then positional key."""
+        return self.d_c + self.d_rope
+
+
+TINY = Dims(d_model=512, n_heads=8, qk_nope=64, d_rope=16, v_head=64, d_c=64)
+DSV2 = Dims(d_model=5120, n_heads=128, qk_nope=128, d_rope=64, v_head=128, d_c=512)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    dims: Dims
+    dtype: str            # "f32" or "bf16"
+    batch: int
+    len_lo: int           # cached tokens per sequence before the step (inclusive bounds)
+    len_hi: int
+    n_q: int              # query tokens per sequence
+    n_append: int         # query tokens appended to the cache before attention (0 or n_q)
+    seed: int
+    fill: str             # "append": cache built with compress_append; "direct": latent rows drawn
+    note: str = ""
+
+    @property
+    def fixed_len(self) -> bool:
+        return self.len_lo == self.len_hi
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("tiny_f32_b1_ctx10", TINY, "f32", 1, 10, 10, 1, 0, 0, "append",
+                 "10 cached tokens built by append at positions 0..9, one query at position 10"),
+        Workload("dsv2_b16_ctx4096", DSV2, "bf16", 16, 4096, 4096, 1, 0, 2, "append",
+                 "cache built by appending 65,536 tokens"),
+        Workload("dsv2_b64_ctx1k_8k", DSV2, "bf16", 64, 1024, 8192, 1, 0, 3, "direct",
+                 "ragged lengths"),
+        Workload("dsv2_b64_ctx8192", DSV2, "bf16", 64, 8191, 8191, 1, 1, 33, "direct",
+                 "decode step: 8191 cached + the new token appended = 8192 attended per sequence"),
+        Workload("dsv2_b4_ctx65536", DSV2, "bf16", 4, 65536, 65536, 1, 0, 4, "direct",
+                 "long context, split-KV"),
+        Workload("dsv2_b128_ctx4k_32k_nq2", DSV2, "bf16", 128, 4096, 32768, 2, 2, 5, "direct",
+                 "two new tokens appended, causal between them"),
+    ]
+}
+
+
+# ---------------------------------------------------------------- bf16 helpers
+def round_to_bf16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); returns float32."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    bits = a.view(np.uint32).astype(np.uint64)
+    bias = ((bits >> 16) & 1) + 0x7FFF
+    out = ((bits + bias) & 0xFFFF0000).astype(np.uint32)
+    return out.view(np.float32).reshape(a.shape)
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """uint16 bit patterns of float32 values that are already bf16-exact."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return (a.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def storage(a: np.ndarray, dtype: str) -> np.ndarray:
+    return round_to_bf16(a) if dtype == "bf16" else np.asarray(a, dtype=np.float32)
+
+
+# ---------------------------------------------------------------- draws
+def main_rng(w: Workload) -> np.random.Generator:
+    return np.random.default_rng(w.seed)
+
+
+def _normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+    out = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        out *= np.float32(std)
+    return out
+
+
+def draw_weights(dims: Dims, dtype: str, rng: np.random.Generator) -> dict:
+    """Weights stored [out_features, in_features] (per-head up-projections [H, out, d_c])."""
+    H = dims.n_heads
+    spec = [
+        ("W_DKV", (dims.d_c, dims.d_model), dims.d_model),
+        ("W_KR", (dims.d_rope, dims.d_model), dims.d_model),
+        ("W_Q", (H * dims.qk_nope, dims.d_model), dims.d_model),
+        ("W_QR", (H * dims.d_rope, dims.d_model), dims.d_model),
+        ("W_UK", (H, dims.qk_nope, dims.d_c), dims.d_c),
+        ("W_UV", (H, dims.v_head, dims.d_c), dims.d_c),
+        ("W_O", (dims.d_model, H * dims.v_head), H * dims.v_head),
+    ]
+    return {name: storage(_normal(rng, shape, 1.0 / np.sqrt(fan_in)), dtype) for name, shape, fan_in in spec}
+
+
+def draw_lengths(w: Workload, rng: np.random.Generator) -> np.ndarray:
+    if w.fixed_len:
+        return np.full(w.batch, w.len_lo, dtype=np.int64)
+    return rng.integers(w.len_lo, w.len_hi, size=w.batch, endpoint=True).astype(np.int64)
+
+
+def draw_hidden(rng: np.random.Generator, n: int, d_model: int, dtype: str) -> np.ndarray:
+    return storage(_normal(rng, (n, d_model), 1.0), dtype)
+
+
+def draw_latent_rows(w: Workload, b: int, n_rows: int) -> np.ndarray:
+    """Directly drawn cache rows [n_rows, d_c + d_rope] for sequence b (its own sub-stream)."""
+    rng = np.random.default_rng([w.seed, 1000 + b])
+    return storage(_normal(rng, (n_rows, w.dims.row), 1.0), w.dtype)
+
+
+def draw_block_table(capacity: np.ndarray, block_size: int, rng: np.random.Generator,
+                     spare: int = SPARE_BLOCKS):
+    """Shuffled physical blocks for each sequence's logical blocks.
+
+    Returns (block_table [B, max_blocks] int32 with -1 in unused entries,
+    num_blocks including ``spare`` never-referenced blocks).
+    """
+    nblk = [(int(c) + block_size - 1) // block_size for c in capacity]
+    total = int(sum(nblk))
+    perm = rng.permutation(total).astype(np.int32)
+    max_blocks = max(nblk) if nblk else 0
+    table = np.full((len(capacity), max(max_blocks, 1)), -1, dtype=np.int32)
+    k = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    return table, total + spare
+
+
+@dataclass
+class Problem:
+    """Everything one workload step needs, on the host, in logical (unpaged) order."""
+    w: Workload
+    weights: dict
+    lens: np.ndarray            # cached tokens before the step
+    kv_len: np.ndarray          # tokens in the cache during attention
+    x_ctx: np.ndarray | None    # [sum(lens), d_model] for append-built caches
+    x_q: np.ndarray             # [B * n_q, d_model]
+    q_pos: np.ndarray           # [B * n_q] int32
+    block_table: np.ndarray
+    num_blocks: int
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def dims(self) -> Dims:
+        return self.w.dims
+
+
+def make_problem(w: Workload, with_weights: bool = True) -> Problem:
+    """Draw one workload in the documented order (weights are always drawn so
+    that the stream stays aligned; ``with_weights=False`` only drops them)."""
+    rng = main_rng(w)
+    d = w.dims
+    weights = draw_weights(d, w.dtype, rng)
+    lens = draw_lengths(w, rng)
+    x_ctx = draw_hidden(rng, int(lens.sum()), d.d_model, w.dtype) if w.fill == "append" else None
+    x_q = draw_hidden(rng, w.batch * w.n_q, d.d_model, w.dtype)
+    kv_len = lens + w.n_append
+    table, num_blocks = draw_block_table(kv_len, d.block_size, rng)
+    q_pos = (lens[:, None] + np.arange(w.n_q)[None, :]).reshape(-1).astype(np.int32)
+    if not with_weights:
+        weights = {}
+    return Problem(w, weights, lens, kv_len, x_ctx, x_q, q_pos, table, num_blocks)
+
+
+def paged_slots(block_table: np.ndarray, b: int, positions: np.ndarray, block_size: int) -> np.ndarray:
+    """Physical row index (block * block_size + offset) of logical positions of sequence b."""
+    positions = np.asarray(positions, dtype=np.int64)
+    return block_table[b, positions // block_size].astype(np.int64) * block_size + positions % block_size

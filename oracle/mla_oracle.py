@@ -1,0 +1,288 @@
+"""Float64 CPU oracle for the MLA decode path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this module.  It shares no code with the CUDA
+library and never reads the paged cache layout: it works on logical
+(per-sequence, per-position) rows.
+
+Sources, cited as [tag section] below:
+  [KJ]  "What does Multi-head Latent Attention compress, and how is that
+        different from quantizing the cache?" (katajob.com)
+  [ZQ]  "How does DeepSeek's Multi-Latent Attention (MLA) compress the KV cache
+        below GQA?" (zenaique.com)
+  [BB]  "Multi-head Latent Attention (MLA)" (bembew.net)
+  [TM]  "Multi-head Latent Attention" knowledge card mla-attention (talentme)
+  [SC]  "What Is Multi-head Latent Attention—and How Does It Shrink AI's
+        Memory?" (satishkchoudhary.com, transcript)
+
+Readings where the pages are silent or garbled (each repeated in the design doc):
+  * weights are stored [out, in]; a projection is W @ x             (c8)
+  * one decoupled RoPE key k_R per token, shared by all heads; each
+    head has its own rotated query part q_R                          (c1)
+  * the content key and the RoPE key are concatenated, so a score is
+    the sum of the two dot products                                  (c2)
+  * scale = 1/sqrt(qk_nope + d_rope)                                 (c3)
+  * RoPE rotates interleaved pairs (2i, 2i+1), theta_i = base^(-2i/d_r) (c4)
+  * query j of a sequence sees vis_j = kv_len - (n_q - 1 - j) tokens (c5)
+  * no query compression, no norms, no biases                        (c6)
+  * an empty visible set gives a zero output                         (c10)
+
+Every function computes in float64 on float64 copies of its inputs.
+Parity: every function below is pinned by a test in tests/test_oracle.py
+(brute force, invariants, special cases, closed forms); see the table in
+the design doc.  The only unpinned claim (model quality on real benchmarks) is
+not computed here.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+f64 = np.float64
+
+
+def _a(x) -> np.ndarray:
+    return np.asarray(x, dtype=f64)
+
+
+# ------------------------------------------------------------------ RoPE
+def rope_angles(pos, d_rope: int, base: float = 10000.0) -> np.ndarray:
+    """phi[p, i] = pos_p * base^(-2i/d_rope), i < d_rope/2.
+
+    [BB §2 Decoupling RoPE from Compression]: RoPE injects position by a
+    position-dependent rotation; the frequencies follow reading c4.
+    """
+    pos = _a(pos).reshape(-1)
+    i = np.arange(d_rope // 2, dtype=f64)
+    theta = np.power(f64(base), -2.0 * i / d_rope)
+    return pos[:, None] * theta[None, :]
+
+
+def apply_rope(v, pos, base: float = 10000.0) -> np.ndarray:
+    """Rotate each interleaved pair (v[2i], v[2i+1]) of the last axis by phi_i(pos).
+
+    v: [..., d_rope]; pos broadcast against v's leading axes.
+    [a, b] -> [a cos phi - b sin phi, a sin phi + b cos phi].
+    """
+    v = _a(v)
+    d_rope = v.shape[-1]
+    lead = v.shape[:-1]
+    pos = np.broadcast_to(_a(pos), lead)
+    phi = rope_angles(pos.reshape(-1), d_rope, base).reshape(*lead, d_rope // 2)
+    a, b = v[..., 0::2], v[..., 1::2]
+    cos, sin = np.cos(phi), np.sin(phi)
+    out = np.empty_like(v)
+    out[..., 0::2] = a * cos - b * sin
+    out[..., 1::2] = a * sin + b * cos
+    return out
+
+
+# ------------------------------------------------------------------ projections
+def compress(x, W_DKV, W_KR, pos, base: float = 10000.0):
+    """Latent and decoupled RoPE key of each token: c_t = W_DKV x_t, k_R,t = RoPE(W_KR x_t, pos_t).
+
+    [KJ §The mechanism] down-projection into one latent per token, the only
+    thing retained; [BB §1 eq.] c_KV^t; [BB Implementation Logic] steps 1, 3, 4
+    (latent = h W_down, K_rope = h W_rope, then RoPE); [TM Core Definition] k_t^R.
+    Returns (c [T, d_c], k_R [T, d_rope]).
+    """
+    x = _a(x)
+    c = x @ _a(W_DKV).T
+    k_r = apply_rope(x @ _a(W_KR).T, _a(pos), base)
+    return c, k_r
+
+
+def project_query(x, W_Q, W_QR, q_pos, n_heads: int, base: float = 10000.0):
+    """Per-head content query q_nope^h = W_Q^h x and rotated query q_R^h = RoPE(W_QR^h x, q_pos).
+
+    [KJ §The mechanism] query projection; [ZQ decoupled RoPE question] the
+    positional part is kept out of the absorbable path (reading c1, c6).
+    Returns (q_nope [N, H, qk_nope], q_rope [N, H, d_rope]).
+    """
+    x = _a(x)
+    N = x.shape[0]
+    q_nope = (x @ _a(W_Q).T).reshape(N, n_heads, -1)
+    q_rope_raw = (x @ _a(W_QR).T).reshape(N, n_heads, -1)
+    q_rope = apply_rope(q_rope_raw, _a(q_pos).reshape(N, 1), base)
+    return q_nope, q_rope
+
+
+def reconstruct_kv(c, W_UK, W_UV, h: int):
+    """Explicit per-head key content and value: k_t^h = W_UK^h c_t, v_t^h = W_UV^h c_t.
+
+    [KJ solid answer] up-projections expand the latent into every head's keys
+    and values; [BB §1 eq.] K^t = W c^t, V^t = W c^t (the page's matrix names
+    are garbled; reading c7 treats both as up-projections).
+    """
+    c = _a(c)
+    return c @ _a(W_UK)[h].T, c @ _a(W_UV)[h].T
+
+
+def softmax_scale(qk_nope: int, d_rope: int) -> float:
+    """Reading c3: 1/sqrt of the full explicit key width."""
+    return 1.0 / np.sqrt(qk_nope + d_rope)
+
+
+def visible(kv_len: int, n_q: int, j: int) -> int:
+    """Reading c5: query j of n_q sees the first kv_len - (n_q - 1 - j) cached tokens."""
+    return max(0, int(kv_len) - (n_q - 1 - j))
+
+
+def _softmax_weights(s: np.ndarray):
+    """Max-subtracted softmax over the last axis, float64; also returns log-sum-exp."""
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    z = np.sum(e, axis=-1, keepdims=True)
+    return e / z, (m + np.log(z))[..., 0]
+
+
+# ------------------------------------------------------------------ explicit attention
+def attend_explicit(q_nope, q_rope, c, k_r, W_UK, W_UV, kv_len: int, scale: float | None = None):
+    """Standard multi-head softmax attention for one sequence, with K and V rebuilt per head.
+
+    This is the plain definition the absorbed decode path must reproduce:
+      k_t^h = [W_UK^h c_t || k_R,t],  v_t^h = W_UV^h c_t,
+      s_t^h = scale * (q_nope^h . W_UK^h c_t + q_R^h . k_R,t),  t < vis_j,
+      o^h   = sum_t softmax(s^h)_t v_t^h.
+    [KJ §The mechanism, solid answer]; [BB §1 eq., §2, Implementation Logic
+    step 5: content and positional key combined, reading c2]; [SC] every prior
+    token keeps an entry (no token selection).
+    q_nope [n_q, H, qk_nope], q_rope [n_q, H, d_rope], c [L, d_c], k_r [L, d_rope].
+    Returns o [n_q, H, v_head].
+    """
+    q_nope, q_rope, c, k_r = _a(q_nope), _a(q_rope), _a(c), _a(k_r)
+    n_q, H, _ = q_nope.shape
+    if scale is None:
+        scale = softmax_scale(q_nope.shape[-1], q_rope.shape[-1])
+    v_head = _a(W_UV).shape[1]
+    out = np.zeros((n_q, H, v_head), dtype=f64)
+    for h in range(H):
+        K_h, V_h = reconstruct_kv(c, W_UK, W_UV, h)       # [L, qk_nope], [L, v_head]
+        for j in range(n_q):
+            vis = visible(kv_len, n_q, j)
+            if vis == 0:
+                continue                                   # reading c10
+            s = scale * (K_h[:vis] @ q_nope[j, h] + k_r[:vis] @ q_rope[j, h])
+            p, _ = _softmax_weights(s)
+            out[j, h] = p @ V_h[:vis]
+    return out
+
+
+def output_project(o, W_O):
+    """out = W_O concat_h(o^h).  [KJ §Why it is not just extra work] output projection."""
+    o = _a(o)
+    N = o.shape[0]
+    return o.reshape(N, -1) @ _a(W_O).T
+
+
+# ------------------------------------------------------------------ absorbed (latent) form
+def absorb_query(q_nope, W_UK):
+    """q_abs^h = W_UK^h^T q_nope^h, so that q_abs^h . c_t = q_nope^h . (W_UK^h c_t).
+
+    [KJ §Why it is not just extra work]: the key up-projection is folded into
+    the query; [ZQ concept explanation]: reconstruction fused into the
+    attention matmuls.  q_nope [N, H, qk_nope] -> [N, H, d_c].
+    """
+    return np.einsum("nhi,hic->nhc", _a(q_nope), _a(W_UK))
+
+
+def attend_latent(q_abs, q_rope, c, k_r, kv_len: int, scale: float):
+    """Attention scored and accumulated in latent space for one sequence.
+
+      s_t^h = scale * (q_abs^h . c_t + q_R^h . k_R,t),  t < vis_j
+      o_lat^h = sum_t softmax(s^h)_t c_t,  lse^h = log sum_t exp(s_t^h)
+    [KJ §Why it is not just extra work]: after folding, attention runs in
+    the latent space directly and per-head K, V are never formed.
+    q_abs [n_q, H, d_c], q_rope [n_q, H, d_rope] -> (o_lat [n_q, H, d_c], lse [n_q, H]).
+    An empty visible set gives o_lat = 0 and lse = -inf (reading c10).
+    """
+    q_abs, q_rope, c, k_r = _a(q_abs), _a(q_rope), _a(c), _a(k_r)
+    n_q, H, d_c = q_abs.shape
+    o_lat = np.zeros((n_q, H, d_c), dtype=f64)
+    lse = np.full((n_q, H), -np.inf, dtype=f64)
+    for j in range(n_q):
+        vis = visible(kv_len, n_q, j)
+        if vis == 0:
+            continue
+        s = scale * (q_abs[j] @ c[:vis].T + q_rope[j] @ k_r[:vis].T)   # [H, vis]
+        p, lse[j] = _softmax_weights(s)
+        o_lat[j] = p @ c[:vis]
+    return o_lat, lse
+
+
+def up_project_values(o_lat, W_UV):
+    """o^h = W_UV^h o_lat^h: the value up-projection applied after the weighted sum.
+
+    [KJ §Why it is not just extra work]: the value up-projection is folded
+    into the output side.  o_lat [N, H, d_c] -> [N, H, v_head].
+    """
+    return np.einsum("hvc,nhc->nhv", _a(W_UV), _a(o_lat))
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine attention results over disjoint token ranges of one query.
+
+    o = sum_s exp(lse_s - lse) o_s, lse = log sum_s exp(lse_s).  This is the
+    exact identity softmax over a union = weighted softmaxes over the parts.
+    o_parts [S, ..., d], lse_parts [S, ...].
+    """
+    o_parts, lse_parts = _a(o_parts), _a(lse_parts)
+    m = np.max(lse_parts, axis=0)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    w = np.exp(lse_parts - m_safe)
+    z = np.sum(w, axis=0)
+    lse = np.where(z > 0, m_safe + np.log(np.where(z > 0, z, 1.0)), -np.inf)
+    o = np.sum(w[..., None] * o_parts, axis=0) / np.where(z > 0, z, 1.0)[..., None]
+    return o, lse
+
+
+# ------------------------------------------------------------------ whole layer
+def decode_layer_explicit(x_q, q_pos, caches, W, dims, n_q: int, kv_len):
+    """End-to-end explicit form for a batch: query projection, per-head MHA over
+    rebuilt K/V, output projection.  caches[b] = (c [L_b, d_c], k_r [L_b, d_rope])."""
+    q_nope, q_rope = project_query(x_q, W["W_Q"], W["W_QR"], q_pos, dims.n_heads, dims.rope_base)
+    B = len(caches)
+    o = np.zeros((B * n_q, dims.n_heads, dims.v_head), dtype=f64)
+    scale = softmax_scale(dims.qk_nope, dims.d_rope)
+    for b in range(B):
+        c, k_r = caches[b]
+        sl = slice(b * n_q, (b + 1) * n_q)
+        o[sl] = attend_explicit(q_nope[sl], q_rope[sl], c, k_r, W["W_UK"], W["W_UV"], int(kv_len[b]), scale)
+    return output_project(o, W["W_O"])
+
+
+def decode_layer_absorbed(x_q, q_pos, caches, W, dims, n_q: int, kv_len):
+    """The same layer computed the absorbed way (used only as an invariant check)."""
+    q_nope, q_rope = project_query(x_q, W["W_Q"], W["W_QR"], q_pos, dims.n_heads, dims.rope_base)
+    q_abs = absorb_query(q_nope, W["W_UK"])
+    B = len(caches)
+    o_lat = np.zeros((B * n_q, dims.n_heads, dims.d_c), dtype=f64)
+    scale = softmax_scale(dims.qk_nope, dims.d_rope)
+    for b in range(B):
+        c, k_r = caches[b]
+        sl = slice(b * n_q, (b + 1) * n_q)
+        o_lat[sl], _ = attend_latent(q_abs[sl], q_rope[sl], c, k_r, int(kv_len[b]), scale)
+    return output_project(up_project_values(o_lat, W["W_UV"]), W["W_O"])
+
+
+# ------------------------------------------------------------------ cache-size closed forms
+def kv_cache_elems_per_token(n_kv_heads: int, d_head: int, n_layers: int = 1) -> int:
+    """Head-sharing / MHA cache: keys and values per KV head, 2 * H_kv * d per layer.
+
+    [ZQ What MLA caches versus what MHA and GQA cache]; [TM Key Problems
+    Solved] 2Hd per token; [SC] the 32 x 8 x 128 x 2 worked example.
+    """
+    return 2 * n_kv_heads * d_head * n_layers
+
+
+def mla_cache_elems_per_token(d_c: int, d_rope: int, n_layers: int = 1) -> int:
+    """MLA cache: the latent plus the decoupled RoPE key, d_c + d_rope per layer.
+
+    [TM Key Problems Solved] per-token cache d_c; [SC] compact latent plus
+    the smaller positional component; [ZQ] the latent is the only content
+    written to the cache.
+    """
+    return (d_c + d_rope) * n_layers
+
+
+def cache_bytes(n_tokens: int, elems_per_token: int, bytes_per_elem: int) -> int:
+    return int(n_tokens) * int(elems_per_token) * int(bytes_per_elem)
