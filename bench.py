@@ -1,0 +1,376 @@
+"""Benchmark of one MLA decode step on the DeepSeek-V2-shaped layer (batch 64, context 8192).
+
+A step is one pass of the whole decode path over one batch: append the new
+token's latent row, project and absorb its query, attend over the paged latent
+cache (with the split-KV merge), and apply the value and output projections.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line.  `value` is cached tokens attended per second over the
+whole job (sum over sequences of the attended length, times ranks, divided by
+the device time of a step).  Several GPUs run independent replicas (each rank
+its own batch; no collective on the data path).  `--impl reference` times the
+float64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import mla_inputs as I  # noqa: E402
+
+METRIC = "MLA decode cached-tokens/s and achieved HBM GB/s (% roofline), b64 ctx8192"
+UNIT = "cached tokens/s"
+DEFAULT_WORKLOAD = "dsv2_b64_ctx8192"
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+DECODE_SOURCES = ["mla_latent_kv_81_b300/csrc/mla_decode_tc.cu", "mla_latent_kv_81_b300/csrc/mla_tc.cu",
+                  "mla_latent_kv_81_b300/csrc/mla_simt.cu"]
+
+
+# ------------------------------------------------------------------ algorithmic work
+def decode_algorithmic(p: I.Problem) -> dict:
+    """Bytes and FLOPs mla_decode_attention must move / perform for one step.
+
+    Per attended (token, query): the cached row once per sequence ((d_c + d_rope)
+    * elem bytes, read once for all heads and both queries), and
+    2 * H * (d_c + d_rope + d_c) FLOPs (scores over the full row, weighted sum
+    over the latent).  Per query row: q read and o_lat written.  Block table:
+    4 B per 64-token block."""
+    d = p.dims
+    eb = 2 if p.w.dtype == "bf16" else 4
+    kv = p.kv_len.astype(np.int64)
+    n_q = p.w.n_q
+    rows = int(kv.sum())
+    vis = int(sum(max(0, int(k) - (n_q - 1 - j)) for k in kv for j in range(n_q)))
+    latent_bytes = rows * d.row * eb
+    q_bytes = p.w.batch * n_q * d.n_heads * d.row * eb
+    o_bytes = p.w.batch * n_q * d.n_heads * d.d_c * eb
+    table_bytes = int(sum((int(k) + d.block_size - 1) // d.block_size for k in kv)) * 4
+    flops = 2 * d.n_heads * (d.row + d.d_c) * vis
+    return dict(bytes=latent_bytes + q_bytes + o_bytes + table_bytes, latent_bytes=latent_bytes, flops=flops,
+                cached_tokens=rows)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        path = os.path.join(ROOT, rel)
+        if os.path.exists(path):
+            with open(path, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, or None when the
+    decode sources changed since those counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("workload") != workload or rec.get("source_sha") != decode_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample(p: I.Problem, budget_s: float, heads_per_step: int | None = None, max_steps: int | None = None):
+    """Time the float64 oracle (explicit form, as it stands) on whole heads of whole
+    sequences of the workload until `budget_s` or `max_steps` is reached.
+    Returns (cached-token equivalents per second, description, threads, step times)."""
+    from oracle import mla_oracle as O
+    d, W = p.dims, p.weights
+    n_q = p.w.n_q
+    H = d.n_heads
+    hps = heads_per_step or H
+    scale = O.softmax_scale(d.qk_nope, d.d_rope)
+    done_tok, elapsed, steps, times = 0.0, 0.0, 0, []
+    b, h0 = 0, 0
+    rows_cache = {}
+    while True:
+        if b not in rows_cache:
+            rows_cache.clear()
+            rows = I.draw_latent_rows(p.w, b, int(p.kv_len[b])).astype(np.float64)
+            rows_cache[b] = rows
+        rows = rows_cache[b]
+        sl = slice(b * n_q, (b + 1) * n_q)
+        hs = slice(h0, min(H, h0 + hps))
+        nh = hs.stop - hs.start
+        t0 = time.perf_counter()
+        q_nope, q_rope = O.project_query(p.x_q[sl], W["W_Q"].reshape(H, d.qk_nope, -1)[hs].reshape(nh * d.qk_nope, -1),
+                                         W["W_QR"].reshape(H, d.d_rope, -1)[hs].reshape(nh * d.d_rope, -1),
+                                         p.q_pos[sl], nh, d.rope_base)
+        O.attend_explicit(q_nope, q_rope, rows[:, :d.d_c], rows[:, d.d_c:], W["W_UK"][hs], W["W_UV"][hs],
+                          int(p.kv_len[b]), scale)
+        dt = time.perf_counter() - t0
+        times.append(dt)
+        elapsed += dt
+        done_tok += float(p.kv_len[b]) * nh / H
+        steps += 1
+        h0 += nh
+        if h0 >= H:
+            h0, b = 0, (b + 1) % p.w.batch
+        if (max_steps is not None and steps >= max_steps) or (max_steps is None and elapsed >= budget_s):
+            break
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or str(len(os.sched_getaffinity(0)))
+    desc = (f"explicit-form oracle (float64, K/V rebuilt per head) over {steps} sample(s) of {hps} head(s) "
+            f"of one sequence each; {done_tok:.0f} cached-token equivalents")
+    return done_tok / elapsed, desc, threads, times
+
+
+# ------------------------------------------------------------------ main paths
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    w = I.WORKLOADS[args.workload]
+    p = I.make_problem(w)
+    heads = 8
+    oracle_sample(p, 0.0, heads_per_step=heads, max_steps=args.warmup)
+    rate, desc, threads, times = oracle_sample(p, 0.0, heads_per_step=heads, max_steps=args.steps)
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, p),
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc + f"; BLAS threads {threads}"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w: I.Workload, p: I.Problem) -> dict:
+    d = w.dims
+    return {"workload": w.name, "batch": w.batch, "ctx": int(p.kv_len.max()), "ctx_min": int(p.kv_len.min()),
+            "n_q": w.n_q, "n_heads": d.n_heads, "d_c": d.d_c, "d_rope": d.d_rope, "d_model": d.d_model,
+            "qk_nope": d.qk_nope, "v_head": d.v_head, "block_size": d.block_size, "paged": "shuffled block table",
+            "l2": "inputs larger than L2 (latent cache and weights each exceed 126 MB; no flush)",
+            "step": "append new token + absorb query + decode attention (+split-KV merge) + output projection"}
+
+
+def run_ours(args, rank: int, world: int):
+    import torch
+    import mla_harness as Hn
+    import mla_latent_kv_81_b300 as M
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    w = I.WORKLOADS[args.workload]
+    p = I.make_problem(w)
+    L = Hn.DeviceLayer(p)
+    L.fill()
+    # the step rewrites the appended rows in place, so every step sees the same cache
+    stream = torch.cuda.current_stream()
+    alg = decode_algorithmic(p)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        L.step(with_lse=False)
+    code, flags = M.mla_get_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status after warm-up: {M.mla_status_string(code)} ({flags})")
+
+    # ---- device-resident timing of K whole steps, with the decode call timed on the same stream
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = M.mla_kernel_launches()
+    t_start.record(stream)
+    for i in range(args.steps):
+        x_q = L.x_q
+        n = x_q.shape[0]
+        if p.w.n_append:
+            M.mla_compress_append(L.cfg, x_q, L.W["W_DKV"], L.W["W_KR"], L.app_seq, L.app_pos, L.rope, L.cache,
+                                  ws=L._ws("c", M.mla_compress_workspace_bytes(L.cfg, n)))
+        M.mla_absorb_query(L.cfg, x_q, L.W["W_Q"], L.W["W_QR"], L.W["W_UK"], L.q_pos, L.rope, L.q,
+                           ws=L._ws("a", M.mla_absorb_workspace_bytes(L.cfg, n)))
+        ev_dec[i][0].record(stream)
+        L.attend(with_lse=False)
+        ev_dec[i][1].record(stream)
+        M.mla_output_project(L.cfg, L.o_lat, L.W["W_UV"], L.W["W_O"], L.out,
+                             ws=L._ws("o", M.mla_output_workspace_bytes(L.cfg, n)))
+    t_end.record(stream)
+    launches = M.mla_kernel_launches() - launches0
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    if dist is not None:
+        t = torch.tensor([ms_total, statistics.mean(dec_ms)], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total, dec_mean = float(t[0]), float(t[1])
+    else:
+        dec_mean = statistics.mean(dec_ms)
+    ms_step = ms_total / args.steps
+    tokens = alg["cached_tokens"] * world
+    value = tokens / (ms_step * 1e-3)
+
+    # ---- end to end through the public API from pinned host buffers
+    x_host = L.x_q.cpu().pin_memory()
+    out_host = torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory()
+    x_dev = torch.empty_like(L.x_q)
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(3, args.steps // 2)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        L.step(x_q=x_dev, with_lse=False)
+        out_host.copy_(L.out, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    code, flags = M.mla_get_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status after timing: {M.mla_status_string(code)} ({flags})")
+
+    hbm_peak, tf_peak, peak_kind = load_peaks()
+    achieved = alg["bytes"] / (dec_mean * 1e-3) / 1e9
+    flops_time = alg["flops"] / (tf_peak * 1e12)
+    bytes_time = alg["bytes"] / (hbm_peak * 1e9)
+    bound = "hbm" if bytes_time >= flops_time else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak}
+    else:
+        ach_tf = alg["flops"] / (dec_mean * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach_tf, "peak": tf_peak, "unit": "TFLOP/s", "frac": ach_tf / tf_peak}
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["kernel"] = "mla_decode_attention (attention kernel + split-KV merge launch), CUDA events on its stream"
+    roof["ms_per_launch"] = dec_mean
+    roof["algorithmic_bytes_per_launch"] = alg["bytes"]
+    roof["algorithmic_flops_per_launch"] = alg["flops"]
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": p.w.dtype, "data": "synthetic (seeded Gaussian activations, weights, latents)",
+        "config": dict(workload_config(w, p), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": roof, "clocks": clk,
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": int(launches),
+    }
+    if not args.no_cpu_baseline:
+        rate, desc, threads, _ = oracle_sample(p, args.cpu_budget, heads_per_step=8)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                "sample": desc + f"; BLAS threads {threads}"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * mla.h - C ABI of the B300 (sm_103a) Multi-head Latent Attention decode library.
+ *
+ * The library computes one MLA attention layer at decode time over a paged
+ * cache that holds, per token, only the latent c_KV (d_c values) and the
+ * decoupled RoPE key k_R (d_rope values).  Per-head keys and values are never
+ * formed: the key up-projection is folded into the query and the value
+ * up-projection is applied after the weighted sum.
+ *
+ * Sources (cited by title and section):
+ *   [KJ] "What does Multi-head Latent Attention compress, and how is that
+ *        different from quantizing the cache?" (katajob.com)
+ *   [ZQ] "How does DeepSeek's Multi-Latent Attention (MLA) compress the KV
+ *        cache below GQA?" (zenaique.com)
+ *   [BB] "Multi-head Latent Attention (MLA)" (bembew.net)
+ *   [TM] "Multi-head Latent Attention" card mla-attention (talentme)
+ *   [SC] "What Is Multi-head Latent Attention—and How Does It Shrink AI's
+ *        Memory?" (satishkchoudhary.com)
+ *
+ * Conventions shared by every call
+ *   - All pointers named d_* or documented as "device" are device pointers on
+ *     the current CUDA device; the caller allocates and owns them.  The
+ *     library never allocates device memory; calls that need scratch take a
+ *     caller-owned workspace whose size the matching *_workspace_bytes()
+ *     returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Argument errors are detected on the host and
+ *     returned before anything is launched.
+ *   - Storage dtype (mla_config.dtype) applies to activations, weights, the
+ *     cache, queries and outputs alike; accumulation is always fp32.  bf16
+ *     results are rounded to nearest even.
+ *   - Weights are stored row-major as [out_features][in_features]; the
+ *     per-head up-projections as [n_heads][out][d_c].
+ *   - Device pointers must be 16-byte aligned.
+ *   - Device-side index problems (a block-table entry outside the pool, a
+ *     position outside a sequence's blocks, a sequence index outside the
+ *     batch) never fault: the offending access is skipped and a flag is set
+ *     that mla_get_device_status() reports.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, inconsistent config        */
+  MLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. odd d_rope)                  */
+  MLA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed                         */
+  MLA_ERR_TIMEOUT = 4,       /* device: a bounded wait gave up (reported by get_device_status) */
+  MLA_ERR_DEVICE_INDEX = 5,  /* device: an out-of-range index was skipped                    */
+  MLA_ERR_WORKSPACE = 6      /* workspace pointer null or smaller than required              */
+} mla_status;
+
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/* Layer shape.  d_rope is the width of both k_R and each head's rotated query
+ * part (qk_rope).  softmax_scale <= 0 selects 1/sqrt(qk_nope + d_rope). */
+typedef struct {
+  int d_model;
+  int n_heads;
+  int qk_nope;
+  int d_rope;
+  int v_head;
+  int d_c;
+  int block_size;      /* tokens per cache block; 64 */
+  float softmax_scale;
+  int dtype;           /* mla_dtype */
+} mla_config;
+
+/* Paged latent cache.  pool: [num_blocks][block_size][d_c + d_rope] of dtype,
+ * each row = [c_KV || k_R] ([ZQ "What MLA caches..."]: the latent is the only
+ * content written to the cache; [SC]: plus the small positional component).
+ * Logical position p of sequence b lives in row
+ *   block_table[b * max_blocks_per_seq + p / block_size] * block_size + p % block_size. */
+typedef struct {
+  void* pool;                   /* device */
+  int num_blocks;
+  const int32_t* block_table;   /* device, [batch][max_blocks_per_seq]; unused entries may hold -1 */
+  int max_blocks_per_seq;
+  int batch;                    /* rows of block_table */
+} mla_paged_cache;
+
+/* RoPE cos/sin table: [max_pos][d_rope/2][2] fp32 (cos, sin of pos * base^(-2i/d_rope)). */
+typedef struct {
+  const float* cos_sin;         /* device */
+  int max_pos;
+} mla_rope_table;
+
+/* Bytes one token occupies in the cache: (d_c + d_rope) * sizeof(dtype).
+ * [TM "Key Problems Solved"]: the per-token cache shrinks from 2*H*d to the
+ * latent; [SC]: plus the positional part.  Returns 0 for an invalid config. */
+size_t mla_cache_bytes_per_token(const mla_config* cfg);
+
+/* Fill a RoPE table on the device for positions [0, max_pos):
+ *   cos_sin[p][i] = (cos(p * base^(-2i/d_rope)), sin(...)), computed in double
+ * precision and rounded to fp32.  Pairs (2i, 2i+1) are rotated together
+ * ([BB "2. Decoupling RoPE from Compression"]; interleaved-pair reading).
+ * d_cos_sin: device, max_pos * d_rope floats. */
+mla_status mla_rope_table_create(const mla_config* cfg, float base, int max_pos, float* d_cos_sin,
+                                 mla_stream_t stream);
+
+/* Workspace bytes mla_compress_append needs for T tokens. */
+size_t mla_compress_workspace_bytes(const mla_config* cfg, int T);
+
+/* Down-project T tokens and write their cache rows.
+ *   c_t   = W_DKV x_t                    ([KJ "The mechanism"]; [BB "1. Low-Rank
+ *                                          Decomposition" and "Implementation Logic" step 1])
+ *   k_R,t = RoPE(W_KR x_t, pos_t)        ([BB "Implementation Logic" steps 3-4];
+ *                                          [TM "Core Definition"] k_t^R)
+ * and store [c_t || k_R,t] at logical position pos[t] of sequence seq_idx[t].
+ *   x      device [T][d_model]
+ *   W_DKV  device [d_c][d_model];  W_KR device [d_rope][d_model]
+ *   seq_idx, pos  device int32 [T]
+ *   rope   table covering every pos[t]
+ *   cache  the paged cache; only the T addressed rows are written
+ * A token whose seq_idx, pos or block id is out of range is skipped and
+ * flagged (MLA_ERR_DEVICE_INDEX via mla_get_device_status). */
+mla_status mla_compress_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
+                               const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
+                               const mla_paged_cache* cache, int T,
+                               void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* Workspace bytes mla_absorb_query needs for N query tokens. */
+size_t mla_absorb_workspace_bytes(const mla_config* cfg, int N);
+
+/* Project N query tokens and fold the key up-projection into them:
+ *   q_nope^h = W_Q^h x,  q_R^h = RoPE(W_QR^h x, q_pos),  q_abs^h = W_UK^h^T q_nope^h
+ * ([KJ "Why it is not just extra work at decode time"]: the key up-projection
+ * is absorbed into the query projection).
+ *   x      device [N][d_model];  q_pos device int32 [N]
+ *   W_Q    device [n_heads*qk_nope][d_model];  W_QR device [n_heads*d_rope][d_model]
+ *   W_UK   device [n_heads][qk_nope][d_c]
+ *   q_out  device [N][n_heads][d_c + d_rope] = [q_abs^h || q_R^h] */
+mla_status mla_absorb_query(const mla_config* cfg, const void* x, const void* W_Q, const void* W_QR,
+                            const void* W_UK, const int32_t* q_pos, const mla_rope_table* rope,
+                            void* q_out, int N, void* workspace, size_t workspace_bytes,
+                            mla_stream_t stream);
+
+/* Workspace bytes mla_decode_attention needs for `batch` sequences of n_q
+ * queries whose block tables have max_blocks_per_seq entries. */
+size_t mla_decode_workspace_bytes(const mla_config* cfg, int batch, int n_q, int max_blocks_per_seq);
+
+/* Softmax attention of every query over the latent cache, accumulated in latent space:
+ *   s_t^h   = scale * (q_abs^h . c_t + q_R^h . k_R,t)   for t < vis_j
+ *   o_lat^h = sum_t softmax(s^h)_t c_t
+ * with vis_j = kv_len[b] - (n_q - 1 - j) for query j of sequence b (causal
+ * among the n_q queries).  Every visible token is attended ([SC]: every prior
+ * token keeps an entry; [ZQ]: decode streams the entire cache from HBM).
+ * Long sequences are split across CTAs and merged by log-sum-exp inside this call.
+ *   q       device [batch][n_q][n_heads][d_c + d_rope] (mla_absorb_query output)
+ *   kv_len  device int32 [batch]; must not exceed max_blocks_per_seq * block_size
+ *   o_lat   device [batch][n_q][n_heads][d_c]
+ *   lse     optional device fp32 [batch][n_q][n_heads] (natural log of the
+ *           softmax normaliser of the scaled scores; -inf when nothing is
+ *           visible), or NULL
+ * A query with no visible token gets o_lat = 0. */
+mla_status mla_decode_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache,
+                                const int32_t* kv_len, int batch, int n_q, void* o_lat, float* lse,
+                                void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* Workspace bytes mla_output_project needs for N query tokens. */
+size_t mla_output_workspace_bytes(const mla_config* cfg, int N);
+
+/* Apply the value up-projection and the output projection:
+ *   o^h = W_UV^h o_lat^h,  out = W_O concat_h(o^h)
+ * ([KJ "Why it is not just extra work at decode time"]: the value
+ * up-projection is absorbed on the output side).
+ *   o_lat  device [N][n_heads][d_c];  W_UV device [n_heads][v_head][d_c]
+ *   W_O    device [d_model][n_heads*v_head];  out device [N][d_model] */
+mla_status mla_output_project(const mla_config* cfg, const void* o_lat, const void* W_UV, const void* W_O,
+                              void* out, int N, void* workspace, size_t workspace_bytes,
+                              mla_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the current device's error word.
+ * Returns MLA_OK, MLA_ERR_DEVICE_INDEX or MLA_ERR_TIMEOUT (the first set);
+ * *flags (if not NULL) receives the raw bit set (bit 0 index, bit 1 timeout). */
+mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags);
+
+/* Number of kernels this library has launched in this process (all devices).
+ * For accounting in benchmarks; no counterpart on the pages. */
+uint64_t mla_kernel_launches(void);
+
+/* Static string naming a status code. */
+const char* mla_status_string(mla_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,126 @@
+"""Device-side set-up for tests, the benchmark and the smoke check.
+
+Uploads a drawn workload (mla_inputs.Problem) to the GPU, lays out the paged
+cache and runs one decode step through the library's C ABI.  Contains no
+attention arithmetic of its own.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import mla_inputs as I
+import mla_latent_kv_81_b300 as M
+
+
+def tdtype(dtype: str):
+    return torch.bfloat16 if dtype == "bf16" else torch.float32
+
+
+def to_dev(a: np.ndarray, dtype: str, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=tdtype(dtype))
+
+
+class DeviceLayer:
+    """One MLA layer's weights, paged cache and RoPE table on the device."""
+
+    def __init__(self, p: I.Problem, device="cuda", max_pos: int | None = None):
+        self.p = p
+        w, d = p.w, p.dims
+        self.device = device
+        self.dt = tdtype(w.dtype)
+        self.cfg = M.make_config(d, w.dtype)
+        self.W = {k: to_dev(v, w.dtype, device) for k, v in p.weights.items()}
+        self.pool = torch.full((p.num_blocks, d.block_size, d.row), float("nan"), dtype=self.dt, device=device)
+        self.block_table = torch.from_numpy(p.block_table).to(device)
+        if max_pos is None:
+            max_pos = int(p.block_table.shape[1]) * d.block_size + 8
+        self.rope_tab = torch.empty((max_pos, d.d_rope // 2, 2), dtype=torch.float32, device=device)
+        M.mla_rope_table_create(self.cfg, d.rope_base, max_pos, self.rope_tab)
+        self.rope = M.make_rope(self.rope_tab)
+        self.cache = M.make_cache(self.pool, self.block_table, d.block_size)
+        self.kv_len = torch.from_numpy(p.kv_len.astype(np.int32)).to(device)
+        self.x_q = to_dev(p.x_q, w.dtype, device)
+        self.q_pos = torch.from_numpy(p.q_pos).to(device)
+        n = p.w.batch * p.w.n_q
+        self.q = torch.empty((n, d.n_heads, d.row), dtype=self.dt, device=device)
+        self.o_lat = torch.empty((n, d.n_heads, d.d_c), dtype=self.dt, device=device)
+        self.lse = torch.empty((n, d.n_heads), dtype=torch.float32, device=device)
+        self.out = torch.empty((n, d.d_model), dtype=self.dt, device=device)
+        # the query tokens appended before attention (their hidden states are the queries)
+        if p.w.n_append:
+            self.app_seq = torch.from_numpy(np.repeat(np.arange(p.w.batch), p.w.n_q).astype(np.int32)).to(device)
+            self.app_pos = self.q_pos
+        self.ws = {}
+
+    # ---------------------------------------------------------------- cache fill
+    def pool_rows(self):
+        return self.pool.view(-1, self.p.dims.row)
+
+    def fill_direct(self):
+        """Write drawn latent rows at every cached position (no projection involved)."""
+        p, d = self.p, self.p.dims
+        flat = self.pool_rows()
+        for b in range(p.w.batch):
+            L = int(p.lens[b])
+            if L == 0:
+                continue
+            rows = I.draw_latent_rows(p.w, b, L)
+            slots = I.paged_slots(p.block_table, b, np.arange(L), d.block_size)
+            flat[torch.from_numpy(slots).to(self.device)] = to_dev(rows, p.w.dtype, self.device)
+
+    def fill_by_append(self, chunk: int = 8192):
+        """Build the cache from x_ctx with mla_compress_append (positions 0..L_b-1)."""
+        p = self.p
+        seq = np.repeat(np.arange(p.w.batch), p.lens).astype(np.int32)
+        pos = np.concatenate([np.arange(L) for L in p.lens]).astype(np.int32)
+        for s in range(0, len(seq), chunk):
+            x = to_dev(p.x_ctx[s:s + chunk], p.w.dtype, self.device)
+            M.mla_compress_append(self.cfg, x, self.W["W_DKV"], self.W["W_KR"],
+                                  torch.from_numpy(seq[s:s + chunk]).to(self.device),
+                                  torch.from_numpy(pos[s:s + chunk]).to(self.device), self.rope, self.cache)
+
+    def fill(self):
+        if self.p.w.fill == "direct":
+            self.fill_direct()
+        else:
+            self.fill_by_append()
+
+    # ---------------------------------------------------------------- one decode step
+    def _ws(self, key, nbytes):
+        t = self.ws.get(key)
+        if t is None or t.numel() < nbytes:
+            t = M.workspace(nbytes, self.device)
+            self.ws[key] = t
+        return t
+
+    def step(self, x_q=None, stream=None, with_lse=True):
+        p, cfg = self.p, self.cfg
+        x_q = self.x_q if x_q is None else x_q
+        n = x_q.shape[0]
+        if p.w.n_append:
+            ws = self._ws("c", M.mla_compress_workspace_bytes(cfg, n))
+            M.mla_compress_append(cfg, x_q, self.W["W_DKV"], self.W["W_KR"], self.app_seq, self.app_pos, self.rope,
+                                  self.cache, ws=ws, stream=stream)
+        ws = self._ws("a", M.mla_absorb_workspace_bytes(cfg, n))
+        M.mla_absorb_query(cfg, x_q, self.W["W_Q"], self.W["W_QR"], self.W["W_UK"], self.q_pos, self.rope, self.q,
+                           ws=ws, stream=stream)
+        self.attend(stream=stream, with_lse=with_lse)
+        ws = self._ws("o", M.mla_output_workspace_bytes(cfg, n))
+        M.mla_output_project(cfg, self.o_lat, self.W["W_UV"], self.W["W_O"], self.out, ws=ws, stream=stream)
+        return self.out
+
+    def attend(self, q=None, stream=None, with_lse=True):
+        p = self.p
+        ws = self._ws("d", M.mla_decode_workspace_bytes(self.cfg, p.w.batch, p.w.n_q, self.cache.max_blocks_per_seq))
+        M.mla_decode_attention(self.cfg, self.q if q is None else q, self.cache, self.kv_len, p.w.batch, p.w.n_q,
+                               self.o_lat, self.lse if with_lse else None, ws=ws, stream=stream)
+        return self.o_lat
+
+    # ---------------------------------------------------------------- host copies for the oracle
+    def cache_rows_logical(self, b: int, n: int | None = None) -> np.ndarray:
+        """Rows 0..n-1 of sequence b read back from the pool, as float32 numpy (exact bf16 values)."""
+        p, d = self.p, self.p.dims
+        n = int(p.kv_len[b]) if n is None else n
+        slots = I.paged_slots(p.block_table, b, np.arange(n), d.block_size)
+        return self.pool_rows()[torch.from_numpy(slots).to(self.device)].float().cpu().numpy()

@@ -200,13 +200,16 @@ class Problem:
         return self.w.dims
 
 
-def make_problem(w: Workload, with_weights: bool = True) -> Problem:
+def make_problem(w: Workload, with_weights: bool = True, lens=None) -> Problem:
     """Draw one workload in the documented order (weights are always drawn so
-    that the stream stays aligned; ``with_weights=False`` only drops them)."""
+    that the stream stays aligned; ``with_weights=False`` only drops them).
+    ``lens`` replaces the drawn cached lengths (test cases with chosen raggedness)."""
     rng = main_rng(w)
     d = w.dims
     weights = draw_weights(d, w.dtype, rng)
-    lens = draw_lengths(w, rng)
+    lens_drawn = draw_lengths(w, rng)
+    lens = lens_drawn if lens is None else np.asarray(lens, dtype=np.int64)
+    assert len(lens) == w.batch
     x_ctx = draw_hidden(rng, int(lens.sum()), d.d_model, w.dtype) if w.fill == "append" else None
     x_q = draw_hidden(rng, w.batch * w.n_q, d.d_model, w.dtype)
     kv_len = lens + w.n_append
@@ -221,3 +224,25 @@ def paged_slots(block_table: np.ndarray, b: int, positions: np.ndarray, block_si
     """Physical row index (block * block_size + offset) of logical positions of sequence b."""
     positions = np.asarray(positions, dtype=np.int64)
     return block_table[b, positions // block_size].astype(np.int64) * block_size + positions % block_size
+
+
+# ---------------------------------------------------------------- stage inputs
+def draw_stage_query(dims: Dims, dtype: str, n: int, seed: int, sharp: float = 1.0) -> np.ndarray:
+    """Absorbed query rows [n, H, d_c + d_rope] drawn directly, for testing attention alone.
+
+    The latent part has std 0.5 and the positional part std 1, the spread of
+    W_UK^T W_Q x and W_QR x with the weight scalings above; ``sharp``
+    multiplies both (sharper softmax).
+    """
+    rng = np.random.default_rng([seed, 7])
+    q = rng.standard_normal((n, dims.n_heads, dims.row), dtype=np.float32)
+    q[..., :dims.d_c] *= np.float32(0.5)
+    if sharp != 1.0:
+        q *= np.float32(sharp)
+    return storage(q, dtype)
+
+
+def draw_stage_latent_out(dims: Dims, dtype: str, n: int, seed: int) -> np.ndarray:
+    """Latent attention outputs [n, H, d_c] drawn directly, for testing the output projection alone."""
+    rng = np.random.default_rng([seed, 8])
+    return storage(rng.standard_normal((n, dims.n_heads, dims.d_c), dtype=np.float32), dtype)

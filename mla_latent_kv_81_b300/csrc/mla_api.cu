@@ -1,0 +1,360 @@
+// extern "C" entry points of the MLA decode library: argument validation,
+// workspace carving and kernel dispatch.  The operations themselves are
+// documented in include/mla.h.
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "mla_common.cuh"
+#include "mla_tc.cuh"
+
+namespace mla {
+
+// Device-side error word (bit 0: index skipped, bit 1: bounded wait gave up).
+static __device__ uint32_t g_status_word;
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+// Per-device constants, resolved once with that device current.
+mla_status device_ctx(cudaStream_t stream, Ctx* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MLA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    g_sm_count[dev] = sms;
+  }
+  out->stream = stream;
+  out->status = g_status_ptr[dev];
+  out->sm_count = g_sm_count[dev];
+  out->device = dev;
+  return MLA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+size_t elem_size(int dtype) { return dtype == MLA_BF16 ? 2 : 4; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+mla_status check_cfg(const mla_config* c) {
+  if (!c) return MLA_ERR_INVALID_ARG;
+  if (c->d_model <= 0 || c->n_heads <= 0 || c->qk_nope <= 0 || c->d_rope <= 0 || c->v_head <= 0 || c->d_c <= 0 ||
+      c->block_size <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (c->dtype != MLA_F32 && c->dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+  if (c->d_rope % 2) return MLA_ERR_UNSUPPORTED;
+  if (c->d_c > 512 || c->d_c + c->d_rope > 2048) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+mla_status check_cache(const mla_paged_cache* k) {
+  if (!k || !ok_ptr(k->pool) || !ok_ptr(k->block_table)) return MLA_ERR_INVALID_ARG;
+  if (k->num_blocks <= 0 || k->max_blocks_per_seq <= 0 || k->batch <= 0) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+mla_status check_rope(const mla_rope_table* r) {
+  if (!r || !ok_ptr(r->cos_sin) || r->max_pos <= 0) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+float resolve_scale(const mla_config* c) {
+  return c->softmax_scale > 0.f ? c->softmax_scale : 1.0f / sqrtf((float)(c->qk_nope + c->d_rope));
+}
+
+// Bump allocator over the caller's workspace.
+struct Carve {
+  char* base;
+  size_t used = 0;
+  template <typename P> P* take(size_t bytes) {
+    P* p = reinterpret_cast<P*>(base ? base + used : nullptr);
+    used = align_up(used + bytes, 256);
+    return p;
+  }
+};
+
+// Split plan of the general decode path: enough CTAs to fill the GPU twice.
+void simt_split_plan(const mla_config* c, int batch, int n_q, int max_blocks, int sm_count, int* splits,
+                     int* tokens_per_split) {
+  const long long cap = (long long)max_blocks * c->block_size;
+  const long long ctas = (long long)batch * n_q * ((c->n_heads + 3) / 4);
+  long long s = ctas > 0 ? (2LL * sm_count + ctas - 1) / ctas : 1;
+  const long long max_s = (cap + 255) / 256;
+  if (s > max_s) s = max_s;
+  if (s < 1) s = 1;
+  long long tps = (cap + s - 1) / s;
+  tps = (tps + 31) / 32 * 32;
+  if (tps < 32) tps = 32;
+  *tokens_per_split = (int)tps;
+  *splits = (int)((cap + tps - 1) / tps);
+}
+
+size_t simt_decode_ws(const mla_config* c, int batch, int n_q, int max_blocks, int sm_count) {
+  int splits = 1, tps = 0;
+  simt_split_plan(c, batch, n_q, max_blocks, sm_count, &splits, &tps);
+  if (splits <= 1) return 0;
+  const size_t items = (size_t)batch * n_q;
+  Carve cv{nullptr};
+  cv.take<float>(items * splits * c->n_heads * c->d_c * sizeof(float));
+  cv.take<float>(items * splits * c->n_heads * sizeof(float));
+  return cv.used;
+}
+
+int current_sm_count() {
+  Ctx ctx;
+  if (device_ctx(nullptr, &ctx) != MLA_OK) return 148;
+  return ctx.sm_count;
+}
+
+#define MLA_TRY(expr)                    \
+  do {                                   \
+    mla_status _s = (expr);              \
+    if (_s != MLA_OK) return _s;         \
+  } while (0)
+#define MLA_CUDA(expr)                          \
+  do {                                          \
+    if ((expr) != cudaSuccess) return MLA_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+uint64_t mla_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_DEVICE_INDEX: return "MLA_ERR_DEVICE_INDEX";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+size_t mla_cache_bytes_per_token(const mla_config* cfg) {
+  if (check_cfg(cfg) != MLA_OK) return 0;
+  return (size_t)(cfg->d_c + cfg->d_rope) * elem_size(cfg->dtype);
+}
+
+mla_status mla_rope_table_create(const mla_config* cfg, float base, int max_pos, float* d_cos_sin,
+                                 mla_stream_t stream) {
+  MLA_TRY(check_cfg(cfg));
+  if (!ok_ptr(d_cos_sin) || max_pos <= 0 || !(base > 1.0f)) return MLA_ERR_INVALID_ARG;
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, &ctx));
+  MLA_CUDA(rope_table_fill(ctx, base, max_pos, cfg->d_rope, d_cos_sin));
+  return MLA_OK;
+}
+
+size_t mla_compress_workspace_bytes(const mla_config* cfg, int T) {
+  if (check_cfg(cfg) != MLA_OK || T < 0) return 0;
+  size_t simt = align_up((size_t)T * (cfg->d_c + cfg->d_rope) * sizeof(float), 256);
+  size_t tc = tc_compress_workspace_bytes(cfg, T);
+  return simt > tc ? simt : tc;
+}
+
+mla_status mla_compress_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
+                               const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
+                               const mla_paged_cache* cache, int T, void* workspace, size_t workspace_bytes,
+                               mla_stream_t stream) {
+  MLA_TRY(check_cfg(cfg));
+  if (T < 0) return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (!ok_ptr(x) || !ok_ptr(W_DKV) || !ok_ptr(W_KR) || !ok_ptr(seq_idx) || !ok_ptr(pos)) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_rope(rope));
+  MLA_TRY(check_cache(cache));
+  const size_t need = mla_compress_workspace_bytes(cfg, T);
+  if (workspace_bytes < need || (need && !ok_ptr(workspace))) return MLA_ERR_WORKSPACE;
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, &ctx));
+  if (tc_compress_supported(cfg, T)) {
+    MLA_CUDA(tc_compress_append(ctx, cfg, x, W_DKV, W_KR, seq_idx, pos, *rope, *cache, T, workspace));
+    return MLA_OK;
+  }
+  const int d_c = cfg->d_c, d_r = cfg->d_rope, width = d_c + d_r;
+  float* Y = static_cast<float*>(workspace);
+  GemmDesc g{};
+  g.X = x; g.x_rs = cfg->d_model; g.x_gs = 0; g.x_f32 = 0;
+  g.W = W_DKV; g.w_ms = cfg->d_model; g.w_ks = 1; g.w_gs = 0;
+  g.Y = Y; g.y_rs = width; g.y_gs = 0; g.y_f32 = 1;
+  g.R = T; g.M = d_c; g.K = cfg->d_model; g.G = 1;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
+  g.W = W_KR; g.Y = Y + d_c; g.M = d_r;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
+  MLA_CUDA(simt_compress_epilogue(ctx, cfg->dtype, Y, T, d_c, d_r, seq_idx, pos, *rope, *cache, cfg->block_size));
+  return MLA_OK;
+}
+
+size_t mla_absorb_workspace_bytes(const mla_config* cfg, int N) {
+  if (check_cfg(cfg) != MLA_OK || N < 0) return 0;
+  const size_t H = cfg->n_heads;
+  Carve cv{nullptr};
+  cv.take<float>((size_t)N * H * cfg->qk_nope * sizeof(float));
+  cv.take<float>((size_t)N * H * cfg->d_rope * sizeof(float));
+  cv.take<float>((size_t)N * H * cfg->d_c * sizeof(float));
+  size_t tc = tc_absorb_workspace_bytes(cfg, N);
+  return cv.used > tc ? cv.used : tc;
+}
+
+mla_status mla_absorb_query(const mla_config* cfg, const void* x, const void* W_Q, const void* W_QR,
+                            const void* W_UK, const int32_t* q_pos, const mla_rope_table* rope, void* q_out, int N,
+                            void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  MLA_TRY(check_cfg(cfg));
+  if (N < 0) return MLA_ERR_INVALID_ARG;
+  if (N == 0) return MLA_OK;
+  if (!ok_ptr(x) || !ok_ptr(W_Q) || !ok_ptr(W_QR) || !ok_ptr(W_UK) || !ok_ptr(q_pos) || !ok_ptr(q_out))
+    return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_rope(rope));
+  const size_t need = mla_absorb_workspace_bytes(cfg, N);
+  if (workspace_bytes < need || (need && !ok_ptr(workspace))) return MLA_ERR_WORKSPACE;
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, &ctx));
+  if (tc_absorb_supported(cfg, N)) {
+    MLA_CUDA(tc_absorb_query(ctx, cfg, x, W_Q, W_QR, W_UK, q_pos, *rope, q_out, N, workspace));
+    return MLA_OK;
+  }
+  const int H = cfg->n_heads, qn = cfg->qk_nope, d_r = cfg->d_rope, d_c = cfg->d_c;
+  Carve cv{static_cast<char*>(workspace)};
+  float* Yn = cv.take<float>((size_t)N * H * qn * sizeof(float));
+  float* Yr = cv.take<float>((size_t)N * H * d_r * sizeof(float));
+  float* Ya = cv.take<float>((size_t)N * H * d_c * sizeof(float));
+  GemmDesc g{};
+  // q_nope = W_Q x   and   q_rope (unrotated) = W_QR x
+  g.X = x; g.x_rs = cfg->d_model; g.x_f32 = 0;
+  g.W = W_Q; g.w_ms = cfg->d_model; g.w_ks = 1;
+  g.Y = Yn; g.y_rs = (long long)H * qn; g.y_f32 = 1;
+  g.R = N; g.M = H * qn; g.K = cfg->d_model; g.G = 1;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
+  g.W = W_QR; g.Y = Yr; g.y_rs = (long long)H * d_r; g.M = H * d_r;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
+  // q_abs^h[c] = sum_i q_nope^h[i] W_UK[h][i][c]   (batched over heads)
+  GemmDesc a{};
+  a.X = Yn; a.x_rs = (long long)H * qn; a.x_gs = qn; a.x_f32 = 1;
+  a.W = W_UK; a.w_ms = 1; a.w_ks = d_c; a.w_gs = (long long)qn * d_c;
+  a.Y = Ya; a.y_rs = (long long)H * d_c; a.y_gs = d_c; a.y_f32 = 1;
+  a.R = N; a.M = d_c; a.K = qn; a.G = H;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, a));
+  MLA_CUDA(simt_query_epilogue(ctx, cfg->dtype, Ya, Yr, N, H, d_c, d_r, q_pos, *rope, q_out));
+  return MLA_OK;
+}
+
+size_t mla_decode_workspace_bytes(const mla_config* cfg, int batch, int n_q, int max_blocks_per_seq) {
+  if (check_cfg(cfg) != MLA_OK || batch < 0 || n_q <= 0 || max_blocks_per_seq <= 0) return 0;
+  const int sms = current_sm_count();
+  size_t simt = simt_decode_ws(cfg, batch, n_q, max_blocks_per_seq, sms);
+  size_t tc = tc_decode_workspace_bytes(cfg, batch, n_q, max_blocks_per_seq, sms);
+  return simt > tc ? simt : tc;
+}
+
+mla_status mla_decode_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache,
+                                const int32_t* kv_len, int batch, int n_q, void* o_lat, float* lse, void* workspace,
+                                size_t workspace_bytes, mla_stream_t stream) {
+  MLA_TRY(check_cfg(cfg));
+  if (batch < 0 || n_q <= 0) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!ok_ptr(q) || !ok_ptr(kv_len) || !ok_ptr(o_lat) || (lse && !aligned16(lse))) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_cache(cache));
+  if (cache->batch < batch) return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_decode_workspace_bytes(cfg, batch, n_q, cache->max_blocks_per_seq);
+  if (workspace_bytes < need || (need && !ok_ptr(workspace))) return MLA_ERR_WORKSPACE;
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, &ctx));
+  const float scale = resolve_scale(cfg);
+  if (tc_decode_supported(cfg, batch, n_q)) {
+    MLA_CUDA(tc_decode_attention(ctx, cfg, q, *cache, kv_len, batch, n_q, scale, o_lat, lse, workspace));
+    return MLA_OK;
+  }
+  int splits = 1, tps = 0;
+  simt_split_plan(cfg, batch, n_q, cache->max_blocks_per_seq, ctx.sm_count, &splits, &tps);
+  const size_t items = (size_t)batch * n_q;
+  Carve cv{static_cast<char*>(workspace)};
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  if (splits > 1) {
+    part_o = cv.take<float>(items * splits * cfg->n_heads * cfg->d_c * sizeof(float));
+    part_lse = cv.take<float>(items * splits * cfg->n_heads * sizeof(float));
+  }
+  MLA_CUDA(simt_decode(ctx, cfg->dtype, q, *cache, cfg->block_size, kv_len, batch, n_q, cfg->n_heads, cfg->d_c,
+                       cfg->d_rope, scale, splits, tps, part_o, part_lse, o_lat, lse));
+  if (splits > 1)
+    MLA_CUDA(combine_partials(ctx, cfg->dtype, part_o, part_lse, (int)items, splits, cfg->n_heads, cfg->d_c, o_lat,
+                              lse));
+  return MLA_OK;
+}
+
+size_t mla_output_workspace_bytes(const mla_config* cfg, int N) {
+  if (check_cfg(cfg) != MLA_OK || N < 0) return 0;
+  size_t simt = align_up((size_t)N * cfg->n_heads * cfg->v_head * sizeof(float), 256);
+  size_t tc = tc_output_workspace_bytes(cfg, N);
+  return simt > tc ? simt : tc;
+}
+
+mla_status mla_output_project(const mla_config* cfg, const void* o_lat, const void* W_UV, const void* W_O, void* out,
+                              int N, void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  MLA_TRY(check_cfg(cfg));
+  if (N < 0) return MLA_ERR_INVALID_ARG;
+  if (N == 0) return MLA_OK;
+  if (!ok_ptr(o_lat) || !ok_ptr(W_UV) || !ok_ptr(W_O) || !ok_ptr(out)) return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_output_workspace_bytes(cfg, N);
+  if (workspace_bytes < need || (need && !ok_ptr(workspace))) return MLA_ERR_WORKSPACE;
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, &ctx));
+  if (tc_output_supported(cfg, N)) {
+    MLA_CUDA(tc_output_project(ctx, cfg, o_lat, W_UV, W_O, out, N, workspace));
+    return MLA_OK;
+  }
+  const int H = cfg->n_heads, v = cfg->v_head, d_c = cfg->d_c;
+  float* Yo = static_cast<float*>(workspace);
+  // o^h[v] = sum_c W_UV[h][v][c] o_lat^h[c]   (batched over heads)
+  GemmDesc a{};
+  a.X = o_lat; a.x_rs = (long long)H * d_c; a.x_gs = d_c; a.x_f32 = 0;
+  a.W = W_UV; a.w_ms = d_c; a.w_ks = 1; a.w_gs = (long long)v * d_c;
+  a.Y = Yo; a.y_rs = (long long)H * v; a.y_gs = v; a.y_f32 = 1;
+  a.R = N; a.M = v; a.K = d_c; a.G = H;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, a));
+  // out = W_O concat_h o^h
+  GemmDesc g{};
+  g.X = Yo; g.x_rs = (long long)H * v; g.x_f32 = 1;
+  g.W = W_O; g.w_ms = (long long)H * v; g.w_ks = 1;
+  g.Y = out; g.y_rs = cfg->d_model; g.y_f32 = 0;
+  g.R = N; g.M = cfg->d_model; g.K = H * v; g.G = 1;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
+  return MLA_OK;
+}
+
+mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags) {
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, &ctx));
+  MLA_CUDA(cudaStreamSynchronize(stream));
+  uint32_t word = 0;
+  MLA_CUDA(cudaMemcpy(&word, ctx.status, sizeof(word), cudaMemcpyDeviceToHost));
+  const uint32_t zero = 0;
+  MLA_CUDA(cudaMemcpy(ctx.status, &zero, sizeof(zero), cudaMemcpyHostToDevice));
+  if (flags) *flags = word;
+  if (word & kFlagIndex) return MLA_ERR_DEVICE_INDEX;
+  if (word & kFlagTimeout) return MLA_ERR_TIMEOUT;
+  return MLA_OK;
+}
+
+}  // extern "C"

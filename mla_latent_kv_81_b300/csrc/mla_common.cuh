@@ -1,0 +1,75 @@
+// Shared device helpers and internal launcher declarations for the MLA library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla.h"
+
+namespace mla {
+
+enum : uint32_t { kFlagIndex = 1u, kFlagTimeout = 2u };
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+using bf16 = __nv_bfloat16;
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<bf16>(bf16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// Host-side count of kernel launches (see mla_kernel_launches()).
+void count_launch(int n = 1);
+
+__device__ __forceinline__ void flag_error(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
+
+// Resolved logical -> physical row of the paged cache, or -1 (and a flag) when
+// any index is out of range.
+__device__ __forceinline__ long long cache_row(const int32_t* table, int max_blocks, int num_blocks,
+                                               int block_size, int b, int pos) {
+  if (pos < 0 || pos >= max_blocks * block_size) return -1;
+  int blk = table[(long long)b * max_blocks + pos / block_size];
+  if (blk < 0 || blk >= num_blocks) return -1;
+  return (long long)blk * block_size + pos % block_size;
+}
+
+// ------------------------------------------------------------------ launch plumbing
+struct Ctx {
+  cudaStream_t stream;
+  uint32_t* status;   // device error word of the current device
+  int sm_count;
+  int device;
+};
+
+// Generic strided GEMM description: Y[g][r][m] = sum_k X[g][r][k] * W[g][m][k]
+// where W is addressed as W + g*w_gs + m*w_ms + k*w_ks (so both [m][k] and
+// [k][m] weight layouts are expressible).
+struct GemmDesc {
+  const void* X; long long x_rs, x_gs; int x_f32;   // X element type: fp32 or the storage dtype
+  const void* W; long long w_ms, w_ks, w_gs;
+  void* Y; long long y_rs, y_gs; int y_f32;         // Y element type: fp32 or the storage dtype
+  int R, M, K, G;
+};
+
+// SIMT kernels (any shape, fp32 or bf16 storage).
+cudaError_t simt_gemm(const Ctx&, int dtype, const GemmDesc&);
+cudaError_t simt_compress_epilogue(const Ctx&, int dtype, const float* Y, int T, int d_c, int d_r,
+                                   const int32_t* seq_idx, const int32_t* pos, const mla_rope_table& rope,
+                                   const mla_paged_cache& cache, int block_size);
+cudaError_t simt_query_epilogue(const Ctx&, int dtype, const float* Y_abs, const float* Y_rope, int N, int H,
+                                int d_c, int d_r, const int32_t* q_pos, const mla_rope_table& rope, void* q_out);
+cudaError_t simt_decode(const Ctx&, int dtype, const void* q, const mla_paged_cache& cache, int block_size,
+                        const int32_t* kv_len, int B, int n_q, int H, int d_c, int d_r, float scale,
+                        int splits, int tokens_per_split, float* part_o, float* part_lse, void* o_lat,
+                        float* lse_out);
+cudaError_t combine_partials(const Ctx&, int dtype, const float* part_o, const float* part_lse, int items,
+                             int splits, int H, int d_c, void* o_lat, float* lse_out);
+cudaError_t rope_table_fill(const Ctx&, float base, int max_pos, int d_rope, float* cos_sin);
+
+}  // namespace mla

@@ -1,0 +1,116 @@
+"""The C ABI on the host: the library loads, exports every symbol include/mla.h
+declares, reports the per-token cache bytes of the closed form, and rejects bad
+arguments before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_inputs as I
+import mla_latent_kv_81_b300 as M
+from oracle import mla_oracle as O
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mla.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 12
+    for name in names:
+        assert hasattr(M.lib, name), name
+    assert set(M.EXPORTED) == set(names)
+
+
+def test_status_strings():
+    for code, name in M._binding.STATUS.items():
+        assert M.mla_status_string(code) == name
+    assert M.mla_status_string(99) == "MLA_ERR_UNKNOWN"
+
+
+def test_cache_bytes_per_token_matches_closed_form():
+    for dims, dtype, nbytes in ((I.DSV2, "bf16", 2), (I.TINY, "f32", 4)):
+        cfg = M.make_config(dims, dtype)
+        expect = O.cache_bytes(1, O.mla_cache_elems_per_token(dims.d_c, dims.d_rope), nbytes)
+        assert M.mla_cache_bytes_per_token(cfg) == expect
+    assert M.mla_cache_bytes_per_token(M.make_config(I.DSV2, "bf16")) == 1152
+    assert M.mla_cache_bytes_per_token(M.make_config(I.TINY, "f32")) == 320
+
+
+def test_invalid_config_is_rejected():
+    cfg = M.make_config(I.TINY, "f32")
+    cfg.d_rope = 15
+    assert M.mla_cache_bytes_per_token(cfg) == 0
+    cfg = M.make_config(I.TINY, "f32")
+    cfg.dtype = 7
+    assert M.mla_cache_bytes_per_token(cfg) == 0
+    cfg = M.make_config(I.TINY, "f32")
+    cfg.n_heads = 0
+    assert M.mla_compress_workspace_bytes(cfg, 4) == 0
+
+
+def test_workspace_sizes_cover_the_fp32_intermediates():
+    for dims, dtype in ((I.TINY, "f32"), (I.DSV2, "bf16")):
+        cfg = M.make_config(dims, dtype)
+        assert M.mla_compress_workspace_bytes(cfg, 100) >= 100 * dims.row * 4
+        H = dims.n_heads
+        assert M.mla_absorb_workspace_bytes(cfg, 10) >= 10 * H * (dims.qk_nope + dims.d_rope + dims.d_c) * 4
+        assert M.mla_output_workspace_bytes(cfg, 10) >= 10 * H * dims.v_head * 4
+        assert M.mla_decode_workspace_bytes(cfg, 4, 1, 1024) >= 0
+
+
+def _fake(n):
+    return ctypes.c_void_p(0x10000 * n)  # aligned, never dereferenced: validation fails first
+
+
+def test_bad_arguments_fail_before_any_launch():
+    lib = M.lib
+    cfg = M.make_config(I.TINY, "f32")
+    rope = M.mla_rope_table(0x1000, 16)
+    cache = M.mla_paged_cache(0x2000, 4, 0x3000, 2, 1)
+    INV, WS = 1, 6
+    byref = ctypes.byref
+    # null activation pointer
+    assert lib.mla_compress_append(byref(cfg), None, _fake(1), _fake(2), _fake(3), _fake(4), byref(rope),
+                                   byref(cache), 8, _fake(5), 1 << 20, None) == INV
+    # misaligned weight pointer
+    assert lib.mla_compress_append(byref(cfg), _fake(1), ctypes.c_void_p(0x10008), _fake(2), _fake(3), _fake(4),
+                                   byref(rope), byref(cache), 8, _fake(5), 1 << 20, None) == INV
+    # negative token count
+    assert lib.mla_compress_append(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope),
+                                   byref(cache), -1, _fake(6), 1 << 20, None) == INV
+    # zero tokens is a no-op even with null pointers
+    assert lib.mla_compress_append(byref(cfg), None, None, None, None, None, None, None, 0, None, 0, None) == 0
+    # workspace too small
+    assert lib.mla_compress_append(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope),
+                                   byref(cache), 8, _fake(6), 16, None) == WS
+    # empty cache description
+    bad_cache = M.mla_paged_cache(0x2000, 0, 0x3000, 2, 1)
+    assert lib.mla_compress_append(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope),
+                                   byref(bad_cache), 8, _fake(6), 1 << 20, None) == INV
+    # decode: batch larger than the block table
+    assert lib.mla_decode_attention(byref(cfg), _fake(1), byref(cache), _fake(2), 3, 1, _fake(3), None, _fake(4),
+                                    1 << 30, None) == INV
+    # decode: n_q = 0
+    assert lib.mla_decode_attention(byref(cfg), _fake(1), byref(cache), _fake(2), 1, 0, _fake(3), None, _fake(4),
+                                    1 << 30, None) == INV
+    # decode: misaligned lse
+    assert lib.mla_decode_attention(byref(cfg), _fake(1), byref(cache), _fake(2), 1, 1, _fake(3),
+                                    ctypes.c_void_p(0x10004), _fake(4), 1 << 30, None) == INV
+    # absorb / output: null output
+    assert lib.mla_absorb_query(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope), None, 4,
+                                _fake(6), 1 << 30, None) == INV
+    assert lib.mla_output_project(byref(cfg), _fake(1), _fake(2), _fake(3), None, 4, _fake(6), 1 << 30, None) == INV
+    # rope table: non-positive max_pos
+    assert lib.mla_rope_table_create(byref(cfg), 10000.0, 0, _fake(1), None) == INV
+    # unsupported: odd RoPE width
+    odd = M.make_config(I.TINY, "f32")
+    odd.d_rope = 15
+    assert lib.mla_output_project(byref(odd), _fake(1), _fake(2), _fake(3), _fake(4), 4, _fake(6), 1 << 30,
+                                  None) == 2
