@@ -44,6 +44,30 @@ def _a(x) -> np.ndarray:
     return np.asarray(x, dtype=f64)
 
 
+# ------------------------------------------------------------------ storage rounding
+def round_bf16(x) -> np.ndarray:
+    """Nearest bfloat16 value of each element (ties to even), returned as float64.
+
+    bfloat16 keeps 8 significant bits: for |x| in [2^e, 2^(e+1)) the spacing is
+    2^(e-7).  Used only where the bf16 pipeline stores a value (reading c9:
+    cached c and k_R, the absorbed query, the latent output), to give each stage
+    check the inputs the method specifies.
+    """
+    x = _a(x)
+    out = np.zeros_like(x)
+    nz = (x != 0) & np.isfinite(x)
+    ax = np.abs(x[nz])
+    e = np.floor(np.log2(ax))
+    spacing = np.power(2.0, e - 7)
+    q = ax / spacing                       # in [128, 256)
+    r = np.floor(q)
+    frac = q - r
+    r = np.where(frac > 0.5, r + 1, np.where(frac < 0.5, r, r + (r % 2)))
+    out[nz] = np.sign(x[nz]) * r * spacing
+    out[~np.isfinite(x)] = x[~np.isfinite(x)]
+    return out
+
+
 # ------------------------------------------------------------------ RoPE
 def rope_angles(pos, d_rope: int, base: float = 10000.0) -> np.ndarray:
     """phi[p, i] = pos_p * base^(-2i/d_rope), i < d_rope/2.

@@ -10,7 +10,17 @@ F32_TOL = 1e-4   # max |g - o| / max(|o|, RMS(o))
 BF16_TOL = 2e-2  # max |g - o| / RMS(o)
 
 
+def bf16_half_ulp(ref) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |ref| (the rounding error of storing ref in bf16)."""
+    a = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (e - 8), 0.0)
+
+
 def rel_err(got, ref, dtype: str) -> float:
+    """fp32: max |g - o| / max(|o|, RMS(o)).
+    bf16: max (|g - o| - half an ulp of o in bf16) / RMS(o): the result is stored in bf16,
+    so its own final rounding is not counted against the 2e-2 budget."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
@@ -18,7 +28,8 @@ def rel_err(got, ref, dtype: str) -> float:
     if dtype == "f32":
         denom = np.maximum(np.abs(ref), rms)
         return float(np.max(np.abs(got - ref) / denom))
-    return float(np.max(np.abs(got - ref)) / rms)
+    excess = np.maximum(np.abs(got - ref) - bf16_half_ulp(ref), 0.0)
+    return float(np.max(excess) / rms)
 
 
 def assert_close(got, ref, dtype: str, what: str = ""):
@@ -48,7 +59,11 @@ def logical_cache(p: I.Problem, b: int):
 
 
 def oracle_sequence(p: I.Problem, b: int, explicit: bool = True) -> dict:
-    """Everything the oracle says about sequence b of a workload step."""
+    """Everything the oracle says about sequence b of a workload step.
+
+    o_lat / lse are the attention stage's result on the inputs the bf16 method
+    stores (cache rows and absorbed queries rounded to bf16 by the oracle's own
+    rounding, reading c9); `out` is the pure float64 chain from x."""
     d, W = p.dims, p.weights
     n_q = p.w.n_q
     sl = slice(b * n_q, (b + 1) * n_q)
@@ -57,11 +72,13 @@ def oracle_sequence(p: I.Problem, b: int, explicit: bool = True) -> dict:
     q_abs = O.absorb_query(q_nope, W["W_UK"])
     scale = O.softmax_scale(d.qk_nope, d.d_rope)
     kv = int(p.kv_len[b])
-    o_lat, lse = O.attend_latent(q_abs, q_rope, c, k_r, kv, scale)
+    st = O.round_bf16 if p.w.dtype == "bf16" else (lambda v: v)
+    o_lat, lse = O.attend_latent(st(q_abs), st(q_rope), st(c), st(k_r), kv, scale)
     res = dict(c=c, k_r=k_r, q_abs=q_abs, q_rope=q_rope, o_lat=o_lat, lse=lse)
     if explicit:
         o = O.attend_explicit(q_nope, q_rope, c, k_r, W["W_UK"], W["W_UV"], kv, scale)
         res["out"] = O.output_project(o, W["W_O"])
     else:
-        res["out"] = O.output_project(O.up_project_values(o_lat, W["W_UV"]), W["W_O"])
+        o_lat64, _ = O.attend_latent(q_abs, q_rope, c, k_r, kv, scale)
+        res["out"] = O.output_project(O.up_project_values(o_lat64, W["W_UV"]), W["W_O"])
     return res

@@ -273,3 +273,18 @@ def check_cache_closed_forms():
     mla = O.mla_cache_elems_per_token(d_c, 64)
     assert mla == 576 and abs(n / mla - 56.888) < 1e-3
     assert O.mla_cache_elems_per_token(64, 16) == 80 and O.kv_cache_elems_per_token(8, 64) == 1024
+
+
+def check_round_bf16():
+    """The oracle's bf16 rounding against torch's float -> bfloat16 conversion and hand-made ties."""
+    import torch
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 6, 20000), [0.0, -0.0, 1.0, -3.0]])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    # torch rounds the float32 value; compare on inputs that are exact in float32
+    x32 = x.astype(np.float32).astype(np.float64)
+    assert np.array_equal(O.round_bf16(x32), ref)
+    # ties: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 -> even (1); 1 + 3*2^-8 -> 1 + 2^-6
+    assert O.round_bf16(np.array([1 + 2.0 ** -8]))[0] == 1.0
+    assert O.round_bf16(np.array([1 + 3 * 2.0 ** -8]))[0] == 1 + 2.0 ** -6
+    assert O.round_bf16(np.array([-(1 + 2.0 ** -8 + 2.0 ** -20)]))[0] == -(1 + 2.0 ** -7)

@@ -53,3 +53,7 @@ def test_merge_partials():
 
 def test_cache_closed_forms():
     pins.check_cache_closed_forms()
+
+
+def test_round_bf16():
+    pins.check_round_bf16()

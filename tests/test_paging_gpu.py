@@ -2,10 +2,11 @@
 values of the definition (GPU).  Bit-exactness criteria:
   (i)   placement: every row that is not addressed keeps its NaN sentinel bits;
   (ii)  one-hot weights and bf16-exact inputs at position 0: every stored value is exact;
-  (iii) Gaussian inputs: every stored value is within one bf16 ulp of the
-        round-to-nearest-even of the float64 value, and equal to it wherever the
-        float64 value lies farther from a rounding midpoint than the fp32
-        accumulation error bound."""
+  (iii) Gaussian inputs: every stored value is within one bf16 ulp (plus the
+        fp32 accumulation error) of the float64 value, and equal to its
+        round-to-nearest-even wherever the float64 value lies farther from a
+        rounding midpoint than a wide estimate of the fp32 accumulation error
+        (16 * 2u * sqrt(K) * ||w * x||_2, u = 2^-24)."""
 import numpy as np
 import pytest
 import torch
@@ -52,22 +53,23 @@ def test_append_placement_and_values(dims, dtype):
         got = flat[slots].astype(np.float64)
         if dtype == "bf16":
             # (iii) within one ulp everywhere; exact where the fp32 accumulation cannot cross a midpoint
+            # fp32 accumulation error estimate: 2u * sqrt(K) * ||w * x||_2, times a wide safety factor
             xs = p.x_ctx[start - n:start].astype(np.float64)
-            xw = np.abs(xs)
-            u = dims.d_model * 2.0 ** -23
-            acc_c = u * (xw @ np.abs(p.weights["W_DKV"]).T.astype(np.float64))
-            # the rotated pair mixes both unrotated values; add the fp32 table and product roundings
+            u = 2.0 ** -23 * np.sqrt(dims.d_model) * 16
+            acc_c = u * np.sqrt((xs * xs) @ (p.weights["W_DKV"].astype(np.float64) ** 2).T)
             y = xs @ p.weights["W_KR"].T.astype(np.float64)
-            acc_y = u * (xw @ np.abs(p.weights["W_KR"]).T.astype(np.float64))
-            pair = acc_y[:, 0::2] + acc_y[:, 1::2] + 2.0 ** -22 * (np.abs(y[:, 0::2]) + np.abs(y[:, 1::2]))
+            acc_y = u * np.sqrt((xs * xs) @ (p.weights["W_KR"].astype(np.float64) ** 2).T)
+            # a rotated pair mixes both unrotated values; add the fp32 table and product roundings
+            pair = acc_y[:, 0::2] + acc_y[:, 1::2] + 2.0 ** -20 * (np.abs(y[:, 0::2]) + np.abs(y[:, 1::2]))
             acc_bound = np.concatenate([acc_c, np.repeat(pair, 2, axis=1)], axis=1)
             rne = I.round_to_bf16(ref.astype(np.float32)).astype(np.float64)
             ulp = _bf16_ulp(ref)
-            assert np.all(np.abs(got - rne) <= ulp * 1.0001)
+            # within one ulp plus the accumulation estimate everywhere (near-zero values have tiny ulps)
+            assert np.all(np.abs(got - ref) <= ulp + acc_bound)
             lo = np.floor(ref / ulp) * ulp
             dist_mid = np.abs(ref - (lo + ulp / 2))
-            safe = dist_mid > acc_bound * 4
-            assert np.mean(safe) > 0.9
+            safe = dist_mid > acc_bound
+            assert np.mean(safe) > 0.8, np.mean(safe)
             assert np.array_equal(got[safe], rne[safe])
         else:
             err = np.max(np.abs(got - ref) / np.maximum(np.abs(ref), np.sqrt(np.mean(ref ** 2))))

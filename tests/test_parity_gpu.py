@@ -69,9 +69,9 @@ def _stage_decode(dims, dtype, lens, n_q, seed, sharp=1.0, kv_extra=0):
         sl = slice(b * n_q, (b + 1) * n_q)
         ref_o, ref_lse = O.attend_latent(qn[sl, :, :dims.d_c], qn[sl, :, dims.d_c:], rows[:, :dims.d_c],
                                          rows[:, dims.d_c:], int(n), scale)
-        if n - (n_q - 1) <= 0:
-            assert np.all(o[sl] == 0)
-            continue
+        for j in range(n_q):
+            if O.visible(int(n), n_q, j) == 0:
+                assert np.all(o[b * n_q + j] == 0) and np.isneginf(lse[b * n_q + j]).all()
         assert_close(o[sl], ref_o, dtype, f"o_lat[b={b}, L={n}]")
         fin = np.isfinite(ref_lse)
         assert np.all(np.abs(lse[sl][fin] - ref_lse[fin]) <= 1e-3 * (1 + np.abs(ref_lse[fin]))), f"lse b={b}"
