@@ -1,12 +1,8 @@
-// Tensor-core paths: not specialised yet; every call takes the SIMT path.
+// Tensor-core projection paths not specialised yet: those calls take the SIMT path.
 #include "mla_tc.cuh"
 
 namespace mla {
 
-bool tc_decode_supported(const mla_config*, int, int) { return false; }
-size_t tc_decode_workspace_bytes(const mla_config*, int, int, int, int) { return 0; }
-cudaError_t tc_decode_attention(const Ctx&, const mla_config*, const void*, const mla_paged_cache&, const int32_t*,
-                                int, int, float, void*, float*, void*) { return cudaErrorNotSupported; }
 bool tc_compress_supported(const mla_config*, int) { return false; }
 size_t tc_compress_workspace_bytes(const mla_config*, int) { return 0; }
 cudaError_t tc_compress_append(const Ctx&, const mla_config*, const void*, const void*, const void*, const int32_t*,

@@ -168,3 +168,10 @@ def test_device_index_errors_are_flagged_not_faulted():
     code, flags = M.mla_get_device_status()
     assert code == 5
     _status_clean()
+
+
+def test_decode_bf16_general_shape_simt_path():
+    """A bf16 layer whose heads are not the tensor-core-specialised shape takes the general kernels."""
+    dims = I.Dims(d_model=256, n_heads=16, qk_nope=32, d_rope=32, v_head=48, d_c=256)
+    _stage_decode(dims, "bf16", [1, 64, 65, 300], 1, seed=24)
+    _stage_decode(dims, "bf16", [3, 64, 65, 300], 2, seed=25, sharp=4.0)
