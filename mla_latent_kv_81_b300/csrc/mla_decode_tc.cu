@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* kv_le
   const long long T = carry;
   if (threadIdx.x == 0) prefix[items] = carry;
   for (int c = threadIdx.x; c < C; c += kPlanThreads) cluster_range[c] = make_int2(0, 0);
+  // with fewer tiles than clusters, use one cluster per tile so that no cluster's range is empty
+  if (T < C) C = (int)T;
   __syncthreads();
   // pass 2: pieces per query and partial slots
   int carry_p = 0, carry_s = 0;
@@ -261,6 +263,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         uint32_t phase = 0;
         for (int pi = range.x; pi < range.y; ++pi) {
           const Piece pc = p.pieces[pi];
+          if (pc.t_end <= pc.t_begin) continue;
           const int b = pc.item / p.n_q;
           for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
             if (!mbar_wait(&ctrl->k_empty[stage], phase ^ 1, p.status, abort_flag)) goto score_done;
@@ -281,6 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         uint32_t kphase = 0, sphase = 0, qphase = 0;
         for (int pi = range.x; pi < range.y; ++pi) {
           const Piece pc = p.pieces[pi];
+          if (pc.t_end <= pc.t_begin) continue;
           if (!mbar_wait(&ctrl->q_ready, qphase, p.status, abort_flag)) goto score_done;
           qphase ^= 1;
           for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
@@ -307,6 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       uint32_t sphase = 0, pphase = 0;
       for (int pi = range.x; pi < range.y; ++pi) {
         const Piece pc = p.pieces[pi];
+        if (pc.t_end <= pc.t_begin) continue;
         // absorbed query row h -> TMEM columns [kQCol, kQCol + 288)
         {
           const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)pc.item * kH + h) * kRow);
@@ -387,6 +392,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         uint32_t phase = 0;
         for (int pi = range.x; pi < range.y; ++pi) {
           const Piece pc = p.pieces[pi];
+          if (pc.t_end <= pc.t_begin) continue;
           const int b = pc.item / p.n_q;
           for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
             if (!mbar_wait(&ctrl->v_empty[stage], phase ^ 1, p.status, abort_flag)) goto value_done;
@@ -407,6 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       uint32_t vphase = 0, pphase = 0, idle_phase = 0, done_phase = 0;
       for (int pi = range.x; pi < range.y; ++pi) {
         const Piece pc = p.pieces[pi];
+        if (pc.t_end <= pc.t_begin) continue;
         for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
           const int valid = min(kBlk, pc.t_end - t);
           const bool first = (t == pc.t_begin), last = (t + kBlk >= pc.t_end);

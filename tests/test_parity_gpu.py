@@ -69,18 +69,31 @@ def _stage_decode(dims, dtype, lens, n_q, seed, sharp=1.0, kv_extra=0):
         sl = slice(b * n_q, (b + 1) * n_q)
         ref_o, ref_lse = O.attend_latent(qn[sl, :, :dims.d_c], qn[sl, :, dims.d_c:], rows[:, :dims.d_c],
                                          rows[:, dims.d_c:], int(n), scale)
+        seen = [j for j in range(n_q) if O.visible(int(n), n_q, j) > 0]
         for j in range(n_q):
-            if O.visible(int(n), n_q, j) == 0:
+            if j not in seen:
                 assert np.all(o[b * n_q + j] == 0) and np.isneginf(lse[b * n_q + j]).all()
-        assert_close(o[sl], ref_o, dtype, f"o_lat[b={b}, L={n}]")
-        fin = np.isfinite(ref_lse)
-        assert np.all(np.abs(lse[sl][fin] - ref_lse[fin]) <= 1e-3 * (1 + np.abs(ref_lse[fin]))), f"lse b={b}"
+        if not seen:
+            continue
+        rows = [b * n_q + j for j in seen]
+        assert_close(o[rows], ref_o[seen], dtype, f"o_lat[b={b}, L={n}]")
+        assert np.all(np.abs(lse[rows] - ref_lse[seen]) <= 1e-3 * (1 + np.abs(ref_lse[seen]))), f"lse b={b}"
 
 
 @pytest.mark.parametrize("n_q", [1, 2])
 @pytest.mark.parametrize("sharp", [1.0, 8.0])
 def test_decode_bf16_ragged(n_q, sharp):
     _stage_decode(I.DSV2, "bf16", [1, 63, 64, 65, 200, 1000, 4097], n_q, seed=21, sharp=sharp)
+
+
+@pytest.mark.parametrize("lens", [
+    [0, 1, 2],            # fewer tiles than clusters, one query with nothing visible
+    [20000],              # one sequence split across every cluster
+    [64] * 150,           # about two whole tiles per cluster
+    [4096, 0, 17, 8191],  # mixed, with an empty sequence in the middle
+])
+def test_decode_bf16_split_regimes(lens):
+    _stage_decode(I.DSV2, "bf16", lens, 1, seed=26)
 
 
 def test_decode_f32_tiny_shapes_ragged():
