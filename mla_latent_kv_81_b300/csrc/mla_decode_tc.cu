@@ -11,13 +11,12 @@
 // memory, so each unit of work runs on a cluster of two CTAs:
 //   * the score CTA (rank 0) keeps the absorbed query Q [128 x 576] in TMEM,
 //     streams [64 tokens x 576] tiles with TMA, computes S = Q K^T (A from
-//     TMEM), and runs the online softmax with one thread per head row; it
+//     TMEM), and runs the online softmax with two threads per head row; it
 //     pushes bf16 P (and the per-row rescale factor) into the value CTA's
 //     shared memory with st.async;
 //   * the value CTA (rank 1) streams the [64 x 512] latent part of the same
-//     tiles and accumulates O += P V in all 512 TMEM columns; a warpgroup
-//     rescales O when the running maximum jumps (rarely) and writes the
-//     result.
+//     tiles and accumulates O += P V in all 512 TMEM columns; two warpgroups
+//     rescale O when the running maximum jumps (rarely) and write the result.
 // The cached tokens of all queries are cut into equal tile ranges, one per
 // cluster (split-KV); ranges that cover part of a query write fp32 partials
 // that a second kernel merges by log-sum-exp.
@@ -33,23 +32,28 @@ namespace {
 using namespace sm100;
 
 constexpr int kH = 128, kDC = 512, kDR = 64, kRow = 576, kBlk = 64;
-constexpr int kBoxBytes = 64 * 64 * 2;             // one swizzled [64 tokens x 64 elements] box
-constexpr int kKStageBytes = 9 * kBoxBytes;         // score CTA: whole rows (73,728 B)
+constexpr int kThreads = 512;  // warps 0-3: TMA, MMA, TMEM, spare; 4-11: two warpgroups; 12-15: P sender
+constexpr int kBoxBytes = 64 * 64 * 2;             // one swizzled [64 tokens x 64 elements] chunk
+constexpr int kChunks = kRow / 64;                  // 9 chunks per cached row: 8 latent + 1 positional
+constexpr int kKStageBytes = kChunks * kBoxBytes;   // score CTA: whole rows (73,728 B)
 constexpr int kVStageBytes = 8 * kBoxBytes;         // value CTA: latent part (65,536 B)
 constexpr int kKStages = 3;
+constexpr int kKSplit = 5;                          // a score stage loads and frees as chunks 0-4 and chunks 5-8
 constexpr int kVStages = 2;
 constexpr int kPSlots = 3;
-constexpr int kSlotBytes = 18432;                    // P 16 KB + alpha + l + m (padded to 1 KB)
-constexpr int kSlotAlpha = 16384, kSlotL = 16896, kSlotM = 17408;
-constexpr int kCtrlBytes = 2048;
+constexpr int kSlotBytes = 18432;                   // P 16 KB | alpha | l (cols 0-31) | l (cols 32-63) | m
+constexpr int kSlotAlpha = 16384, kSlotL0 = 16896, kSlotL1 = 17408, kSlotM = 17920;
+constexpr int kCtrlBytes = 4096;
 constexpr int kOffStages = kCtrlBytes;                               // both roles
 constexpr int kOffSlots = kOffStages + kVStages * kVStageBytes;     // value CTA
 constexpr int kSmemScore = kOffStages + kKStages * kKStageBytes;
 constexpr int kSmemValue = kOffSlots + kPSlots * kSlotBytes;
 constexpr int kSmemBytes = (kSmemScore > kSmemValue ? kSmemScore : kSmemValue) + 1024;  // + alignment slack
 constexpr uint32_t kTxTile = 16384 + 512;
-constexpr uint32_t kTxLast = kTxTile + 1024;
-constexpr int kSCol = 0, kQCol = 128;                // score CTA TMEM columns: S buffers at 0/64, Q at 128..415
+constexpr uint32_t kTxLast = kTxTile + 1536;
+// score CTA TMEM columns: S buffers at 0 and 64, Q at 128..415, two staged P tiles at 416 and 448
+// (64 bf16 per row packed in 32 columns), per-row alpha / l (two halves) / m of each staged tile at 480 + 4*slot
+constexpr int kSCol = 0, kQCol = 128, kPStageCol = 416, kPExtraCol = 480;
 constexpr float kRescaleThreshold = 8.0f;            // log2 units: rescale O only when the max grows by 2^8
 
 enum : int { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
@@ -62,9 +66,11 @@ struct Piece {
 };
 
 struct Ctrl {
-  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t k_full[kKStages][2], k_empty[kKStages][2];   // [stage][chunks 0-4 | chunks 5-8]
   uint64_t s_full[2], s_empty[2];
   uint64_t q_ready;
+  uint64_t xch[2];
+  uint64_t p_staged[2], p_free[2];
   uint64_t p_empty[kPSlots];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t p_full[kPSlots];
@@ -74,6 +80,7 @@ struct Ctrl {
   int cmd, cmd_slot, cmd_piece;
   float l_buf[kH];
   float m_buf[kH];
+  float half_max[2][2][kH];   // [tile parity][column half][row]
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
@@ -93,6 +100,48 @@ struct Params {
 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Walks the tiles of a cluster's pieces in order.
+struct TileCursor {
+  int pi, end, t, t_end, b;
+  __device__ void start(const Piece* pieces, int first, int last, int n_q) {
+    pi = first - 1;
+    end = last;
+    t = t_end = 0;
+    b = 0;
+    next_piece(pieces, n_q);
+  }
+  __device__ void next_piece(const Piece* pieces, int n_q) {
+    while (++pi < end) {
+      const Piece pc = pieces[pi];
+      if (pc.t_end > pc.t_begin) {
+        t = pc.t_begin;
+        t_end = pc.t_end;
+        b = pc.item / n_q;
+        return;
+      }
+    }
+  }
+  __device__ bool valid() const { return pi < end; }
+  __device__ void advance(const Piece* pieces, int n_q) {
+    t += kBlk;
+    if (t >= t_end) next_piece(pieces, n_q);
+  }
+};
+
+constexpr int kLookahead = 4;   // block-table entries read this many tiles before their loads
+
+// Physical block of the cursor's tile (0 and a flag when the table entry is out of range), or -1 past the end.
+__device__ __forceinline__ int block_of(const TileCursor& c, const int32_t* table, int max_blocks, int num_blocks,
+                                        uint32_t* status, bool flag) {
+  if (!c.valid()) return -1;
+  int blk = __ldg(table + (long long)c.b * max_blocks + c.t / kBlk);
+  if (blk < 0 || blk >= num_blocks) {
+    if (flag) flag_error(status, kFlagIndex);
+    blk = 0;
+  }
+  return blk;
+}
 
 // A wait whose outcome is the same for every lane of the warp (tcgen05 loads and
 // stores that follow are warp-collective).
@@ -215,13 +264,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* kv_le
 }
 
 // ------------------------------------------------------------------ attention kernel
-__device__ __forceinline__ uint64_t k_desc(uint32_t stage_addr, int s) {
-  // K-major B operand: K-step s (16 elements) of the [64 tokens x 576] tile
-  return desc_sw128(stage_addr + (s >> 2) * kBoxBytes + (s & 3) * 32, 16, 1024);
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap pool_map, Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap map5, const __grid_constant__ CUtensorMap map4, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
@@ -231,14 +275,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   volatile int* abort_flag = &ctrl->abort_flag;
 
   if (tid == 0) {
-    for (int i = 0; i < kKStages; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&ctrl->s_full[i], 1); mbar_init(&ctrl->s_empty[i], 128); }
-    mbar_init(&ctrl->q_ready, 128);
+    for (int i = 0; i < kKStages; ++i)
+      for (int j = 0; j < 2; ++j) { mbar_init(&ctrl->k_full[i][j], 1); mbar_init(&ctrl->k_empty[i][j], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctrl->s_full[i], 1);
+      mbar_init(&ctrl->s_empty[i], 256);
+      mbar_init(&ctrl->xch[i], 256);
+      mbar_init(&ctrl->p_staged[i], 256);
+      mbar_init(&ctrl->p_free[i], 128);
+    }
+    mbar_init(&ctrl->q_ready, 256);
     for (int i = 0; i < kPSlots; ++i) { mbar_init(&ctrl->p_empty[i], 1); mbar_init(&ctrl->p_full[i], 1); }
     for (int i = 0; i < kVStages; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
     mbar_init(&ctrl->mma_idle, 1);
     mbar_init(&ctrl->work, 1);
-    mbar_init(&ctrl->done, 128);
+    mbar_init(&ctrl->done, 256);
     ctrl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -246,7 +297,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     tmem_alloc(&ctrl->tmem_base, 512);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&pool_map);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&map5);
+    prefetch_tmap(&map4);
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();
@@ -254,25 +308,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   const uint32_t tmem = ctrl->tmem_base;
   const int2 range = p.cluster_range[cid];
   const uint32_t smem_base = smem_u32(smem);
+  // warpgroup lanes: warps 4..11, quarter q = TMEM lane group, half = which 32 columns / 256 O columns
+  const int q4 = warp & 3, half = (warp - 4) >> 2;
+  const int h = q4 * 32 + lane;
 
   if (rank == 0) {
     // =========================== score CTA ===========================
     if (warp == 0) {
       if (lane == 0) {
+        // block-table entries are read kLookahead tiles ahead so their latency overlaps the stage waits
         int stage = 0;
         uint32_t phase = 0;
-        for (int pi = range.x; pi < range.y; ++pi) {
-          const Piece pc = p.pieces[pi];
-          if (pc.t_end <= pc.t_begin) continue;
-          const int b = pc.item / p.n_q;
-          for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
-            if (!mbar_wait(&ctrl->k_empty[stage], phase ^ 1, p.status, abort_flag)) goto score_done;
-            int blk = p.table[(long long)b * p.max_blocks + t / kBlk];
-            if (blk < 0 || blk >= p.num_blocks) { flag_error(p.status, kFlagIndex); blk = 0; }
-            mbar_arrive_expect_tx(&ctrl->k_full[stage], kKStageBytes);
+        TileCursor ahead;
+        ahead.start(p.pieces, range.x, range.y, p.n_q);
+        int nb[kLookahead];
+#pragma unroll
+        for (int i = 0; i < kLookahead; ++i) {
+          nb[i] = block_of(ahead, p.table, p.max_blocks, p.num_blocks, p.status, true);
+          if (ahead.valid()) ahead.advance(p.pieces, p.n_q);
+        }
+        bool more = nb[0] >= 0;
+        while (more) {
+#pragma unroll
+          for (int u = 0; u < kLookahead; ++u) {
+            const int blk = nb[u];
+            if (blk < 0) { more = false; break; }
+            nb[u] = block_of(ahead, p.table, p.max_blocks, p.num_blocks, p.status, true);
+            if (ahead.valid()) ahead.advance(p.pieces, p.n_q);
             uint8_t* dst = smem + kOffStages + stage * kKStageBytes;
-#pragma unroll 1
-            for (int j = 0; j < 9; ++j) tma_load_3d(dst + j * kBoxBytes, &pool_map, &ctrl->k_full[stage], 64 * j, 0, blk);
+            if (!mbar_wait(&ctrl->k_empty[stage][0], phase ^ 1, p.status, abort_flag)) goto score_done;
+            mbar_arrive_expect_tx(&ctrl->k_full[stage][0], kKSplit * kBoxBytes);
+            tma_load_4d(dst, &map5, &ctrl->k_full[stage][0], 0, 0, 0, blk);
+            if (!mbar_wait(&ctrl->k_empty[stage][1], phase ^ 1, p.status, abort_flag)) goto score_done;
+            mbar_arrive_expect_tx(&ctrl->k_full[stage][1], (kChunks - kKSplit) * kBoxBytes);
+            tma_load_4d(dst + kKSplit * kBoxBytes, &map4, &ctrl->k_full[stage][1], 0, 0, kKSplit, blk);
             if (++stage == kKStages) { stage = 0; phase ^= 1; }
           }
         }
@@ -280,6 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     } else if (warp == 1) {
       if (lane == 0) {
         const uint32_t idesc = idesc_bf16(128, 64, false, false);
+        const uint64_t kdesc0 = desc_sw128(smem_base + kOffStages, 16, 1024);
         int stage = 0, sbuf = 0;
         uint32_t kphase = 0, sphase = 0, qphase = 0;
         for (int pi = range.x; pi < range.y; ++pi) {
@@ -288,35 +358,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           if (!mbar_wait(&ctrl->q_ready, qphase, p.status, abort_flag)) goto score_done;
           qphase ^= 1;
           for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
-            if (!mbar_wait(&ctrl->k_full[stage], kphase, p.status, abort_flag)) goto score_done;
             if (!mbar_wait(&ctrl->s_empty[sbuf], sphase ^ 1, p.status, abort_flag)) goto score_done;
-            tc_fence_after();
-            const uint32_t kaddr = smem_base + kOffStages + stage * kKStageBytes;
+            const uint64_t kd = kdesc0 + (uint64_t)(stage * (kKStageBytes >> 4));
             const uint32_t d = tmem + kSCol + sbuf * 64;
-#pragma unroll 4
-            for (int s = 0; s < kRow / 16; ++s) mma_ts(d, tmem + kQCol + s * 8, k_desc(kaddr, s), idesc, s > 0);
+            // 36 K-steps of 16: chunk s/4 (8 KB apart), 32 B within the 128-B swizzled row;
+            // each half of the stage is released as soon as its MMAs complete
+            if (!mbar_wait(&ctrl->k_full[stage][0], kphase, p.status, abort_flag)) goto score_done;
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < 4 * kKSplit; ++s)
+              mma_ts(d, tmem + kQCol + s * 8, kd + (uint64_t)((s >> 2) * (kBoxBytes >> 4) + (s & 3) * 2), idesc,
+                     s > 0 ? 1u : 0u);
+            mma_commit(&ctrl->k_empty[stage][0]);
+            if (!mbar_wait(&ctrl->k_full[stage][1], kphase, p.status, abort_flag)) goto score_done;
+            tc_fence_after();
+#pragma unroll
+            for (int s = 4 * kKSplit; s < kRow / 16; ++s)
+              mma_ts(d, tmem + kQCol + s * 8, kd + (uint64_t)((s >> 2) * (kBoxBytes >> 4) + (s & 3) * 2), idesc, 1u);
+            mma_commit(&ctrl->k_empty[stage][1]);
             mma_commit(&ctrl->s_full[sbuf]);
-            mma_commit(&ctrl->k_empty[stage]);
             if (++stage == kKStages) { stage = 0; kphase ^= 1; }
             if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
           }
         }
       }
-    } else if (warp >= 4) {
-      // softmax warpgroup: thread h owns head row h (TMEM lane h)
-      const int h = tid - 128;
-      const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      const uint32_t peer_slots = mapa(smem_base + kOffSlots, 1);
-      int sbuf = 0, pslot = 0;
-      uint32_t sphase = 0, pphase = 0;
+    } else if (warp >= 4 && warp < 12) {
+      // softmax: head row h, columns [32*half, 32*half + 32) of each tile
+      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+      int sbuf = 0, tile = 0;
+      uint32_t sphase = 0;
       for (int pi = range.x; pi < range.y; ++pi) {
         const Piece pc = p.pieces[pi];
         if (pc.t_end <= pc.t_begin) continue;
-        // absorbed query row h -> TMEM columns [kQCol, kQCol + 288)
         {
+          // absorbed query row h -> TMEM columns [kQCol, kQCol + 288); chunks 0-4 / 5-8 per half
           const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)pc.item * kH + h) * kRow);
 #pragma unroll 1
-          for (int c = 0; c < 9; ++c) {
+          for (int c = half * 5; c < (half ? 9 : 5); ++c) {
             uint32_t r[32];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -329,55 +407,98 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           tc_fence_before();
           mbar_arrive(&ctrl->q_ready);
         }
-        float m = -INFINITY, l = 0.f;
-        for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
-          const int valid = min(kBlk, pc.t_end - t);
+        float m = -INFINITY, lpart = 0.f;
+        for (int t = pc.t_begin; t < pc.t_end; t += kBlk, ++tile) {
+          const int valid = min(kBlk, pc.t_end - t) - half * 32;   // valid columns in this half (may be <= 0)
           const bool first = (t == pc.t_begin), last = (t + kBlk >= pc.t_end);
           if (!warp_wait(&ctrl->s_full[sbuf], sphase, p.status, abort_flag)) goto score_done;
           tc_fence_after();
-          uint32_t sa[32], sb[32];
-          tmem_ld32(lane_base + kSCol + sbuf * 64, sa);
-          tmem_ld32(lane_base + kSCol + sbuf * 64 + 32, sb);
+          uint32_t sr[32];
+          tmem_ld32(lane_base + kSCol + sbuf * 64 + half * 32, sr);
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&ctrl->s_empty[sbuf]);
           if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
-          float x[64];
-          float mx = -INFINITY;
+          float x[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[i] = i < valid ? __uint_as_float(sa[i]) * p.scale_log2 : -INFINITY;
-            x[i + 32] = i + 32 < valid ? __uint_as_float(sb[i]) * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, fmaxf(x[i], x[i + 32]));
-          }
+          for (int i = 0; i < 32; ++i) x[i] = i < valid ? __uint_as_float(sr[i]) * p.scale_log2 : -INFINITY;
+          float mx8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(fmaxf(x[i], x[i + 8]), fmaxf(x[i + 16], x[i + 24]));
+          const float hmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          // exchange the half-row maxima with the partner thread of the other warpgroup
+          ctrl->half_max[tile & 1][half][h] = hmax;
+          mbar_arrive(&ctrl->xch[tile & 1]);
+          if (!warp_wait(&ctrl->xch[tile & 1], (tile >> 1) & 1, p.status, abort_flag)) goto score_done;
+          const float mx = fmaxf(ctrl->half_max[tile & 1][0][h], ctrl->half_max[tile & 1][1][h]);
           float alpha = 1.f;
           if (first) {
             m = mx;
           } else if (mx > m + kRescaleThreshold) {
             alpha = ex2(m - mx);
-            l *= alpha;
+            lpart *= alpha;
             m = mx;
           }
-          uint32_t pk[32];
-          float psum = 0.f;
+          uint32_t pk[16];
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             const float p0 = ex2(x[2 * i] - m), p1 = ex2(x[2 * i + 1] - m);
-            psum += p0 + p1;
+            ps[i & 3] += p0 + p1;
             pk[i] = pack_bf16x2(p0, p1);
           }
-          l += psum;
+          lpart += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          // stage P and the row statistics in TMEM; the sender warpgroup pushes them to the value CTA
+          const int st = tile & 1;
+          if (!warp_wait(&ctrl->p_free[st], ((tile >> 1) & 1) ^ 1, p.status, abort_flag)) goto score_done;
+          tc_fence_after();
+          tmem_st16(lane_base + kPStageCol + st * 32 + half * 16, pk);
+          if (half == 0) {
+            tmem_st1(lane_base + kPExtraCol + st * 4 + 0, __float_as_uint(alpha));
+            tmem_st1(lane_base + kPExtraCol + st * 4 + 1, __float_as_uint(lpart));
+            tmem_st1(lane_base + kPExtraCol + st * 4 + 3, __float_as_uint(m));
+          } else {
+            tmem_st1(lane_base + kPExtraCol + st * 4 + 2, __float_as_uint(lpart));
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&ctrl->p_staged[st]);
+        }
+      }
+    } else if (warp >= 12) {
+      // P sender: TMEM-staged tiles -> value CTA slots (st.async), row h = lane of this warp's quarter
+      const int hs = (warp & 3) * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      const uint32_t peer_slots = mapa(smem_base + kOffSlots, 1);
+      int pslot = 0, tile = 0;
+      uint32_t pphase = 0;
+      for (int pi = range.x; pi < range.y; ++pi) {
+        const Piece pc = p.pieces[pi];
+        if (pc.t_end <= pc.t_begin) continue;
+        for (int t = pc.t_begin; t < pc.t_end; t += kBlk, ++tile) {
+          const bool last = (t + kBlk >= pc.t_end);
+          const int st = tile & 1;
+          if (!warp_wait(&ctrl->p_staged[st], (tile >> 1) & 1, p.status, abort_flag)) goto score_done;
+          tc_fence_after();
+          uint32_t pk[32], ex[4];
+          tmem_ld32(lane_base + kPStageCol + st * 32, pk);
+          tmem_ld4(lane_base + kPExtraCol + st * 4, ex);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&ctrl->p_free[st]);
           if (!warp_wait(&ctrl->p_empty[pslot], pphase ^ 1, p.status, abort_flag)) goto score_done;
           const uint32_t slot = peer_slots + pslot * kSlotBytes;
           const uint32_t rbar = mapa(smem_u32(&ctrl->p_full[pslot]), 1);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            st_async_v4(slot + h * 128 + ((c ^ (h & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3],
-                        rbar);
-          st_async_b32(slot + kSlotAlpha + 4 * h, __float_as_uint(alpha), rbar);
+            st_async_v4(slot + hs * 128 + ((c ^ (hs & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                        pk[4 * c + 3], rbar);
+          st_async_b32(slot + kSlotAlpha + 4 * hs, ex[0], rbar);
           if (last) {
-            st_async_b32(slot + kSlotL + 4 * h, __float_as_uint(l), rbar);
-            st_async_b32(slot + kSlotM + 4 * h, __float_as_uint(m), rbar);
+            st_async_b32(slot + kSlotL0 + 4 * hs, ex[1], rbar);
+            st_async_b32(slot + kSlotL1 + 4 * hs, ex[2], rbar);
+            st_async_b32(slot + kSlotM + 4 * hs, ex[3], rbar);
           }
           if (++pslot == kPSlots) { pslot = 0; pphase ^= 1; }
         }
@@ -390,18 +511,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       if (lane == 0) {
         int stage = 0;
         uint32_t phase = 0;
-        for (int pi = range.x; pi < range.y; ++pi) {
-          const Piece pc = p.pieces[pi];
-          if (pc.t_end <= pc.t_begin) continue;
-          const int b = pc.item / p.n_q;
-          for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
+        TileCursor ahead;
+        ahead.start(p.pieces, range.x, range.y, p.n_q);
+        int nb[kLookahead];
+#pragma unroll
+        for (int i = 0; i < kLookahead; ++i) {
+          nb[i] = block_of(ahead, p.table, p.max_blocks, p.num_blocks, p.status, false);
+          if (ahead.valid()) ahead.advance(p.pieces, p.n_q);
+        }
+        bool more = nb[0] >= 0;
+        while (more) {
+#pragma unroll
+          for (int u = 0; u < kLookahead; ++u) {
+            const int blk = nb[u];
+            if (blk < 0) { more = false; break; }
+            nb[u] = block_of(ahead, p.table, p.max_blocks, p.num_blocks, p.status, false);
+            if (ahead.valid()) ahead.advance(p.pieces, p.n_q);
             if (!mbar_wait(&ctrl->v_empty[stage], phase ^ 1, p.status, abort_flag)) goto value_done;
-            int blk = p.table[(long long)b * p.max_blocks + t / kBlk];
-            if (blk < 0 || blk >= p.num_blocks) blk = 0;   // flagged by the score CTA
             mbar_arrive_expect_tx(&ctrl->v_full[stage], kVStageBytes);
-            uint8_t* dst = smem + kOffStages + stage * kVStageBytes;
-#pragma unroll 1
-            for (int j = 0; j < 8; ++j) tma_load_3d(dst + j * kBoxBytes, &pool_map, &ctrl->v_full[stage], 64 * j, 0, blk);
+            tma_load_4d(smem + kOffStages + stage * kVStageBytes, &map4, &ctrl->v_full[stage], 0, 0, 0, blk);
+            tma_load_4d(smem + kOffStages + stage * kVStageBytes + 4 * kBoxBytes, &map4, &ctrl->v_full[stage], 0, 0, 4,
+                        blk);
             if (++stage == kVStages) { stage = 0; phase ^= 1; }
           }
         }
@@ -409,6 +539,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     } else if (warp == 1) {
       // MMA warp: lane 0 issues, the whole warp waits and zeroes tail rows
       const uint32_t idesc = idesc_bf16(128, 256, false, true);
+      const uint64_t pdesc0 = desc_sw128(smem_base + kOffSlots, 16, 1024);
+      const uint64_t vdesc0 = desc_sw128(smem_base + kOffStages, kBoxBytes, 1024);
       int vstage = 0, pslot = 0;
       uint32_t vphase = 0, pphase = 0, idle_phase = 0, done_phase = 0;
       for (int pi = range.x; pi < range.y; ++pi) {
@@ -437,9 +569,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           const bool flag = __any_sync(0xffffffffu, alphas[lane] != 1.f || alphas[lane + 32] != 1.f ||
                                                         alphas[lane + 64] != 1.f || alphas[lane + 96] != 1.f);
           if (last) {
+            const float* l0 = reinterpret_cast<const float*>(slot + kSlotL0);
+            const float* l1 = reinterpret_cast<const float*>(slot + kSlotL1);
+            const float* mm = reinterpret_cast<const float*>(slot + kSlotM);
             for (int i = lane; i < kH; i += 32) {
-              ctrl->l_buf[i] = reinterpret_cast<const float*>(slot + kSlotL)[i];
-              ctrl->m_buf[i] = reinterpret_cast<const float*>(slot + kSlotM)[i];
+              ctrl->l_buf[i] = l0[i] + l1[i];
+              ctrl->m_buf[i] = mm[i];
             }
           }
           fence_proxy_async_smem();
@@ -460,13 +595,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t vaddr = smem_u32(vst), paddr = smem_u32(slot);
+            const uint64_t pd = pdesc0 + (uint64_t)(pslot * (kSlotBytes >> 4));
+            const uint64_t vd = vdesc0 + (uint64_t)(vstage * (kVStageBytes >> 4));
 #pragma unroll
             for (int s = 0; s < 4; ++s)
 #pragma unroll
               for (int nh = 0; nh < 2; ++nh)
-                mma_ss(tmem + nh * 256, desc_sw128(paddr + s * 32, 16, 1024),
-                       desc_sw128(vaddr + nh * 4 * kBoxBytes + s * 2048, kBoxBytes, 1024), idesc,
+                mma_ss(tmem + nh * 256, pd + (uint64_t)(s * 2),
+                       vd + (uint64_t)(nh * 4 * (kBoxBytes >> 4) + s * (2048 >> 4)), idesc,
                        (!first || s > 0) ? 1u : 0u);
             mma_commit(&ctrl->v_empty[vstage]);
             mma_commit_multicast(&ctrl->p_empty[pslot], 0x1);
@@ -493,10 +629,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         ctrl->cmd = kCmdExit;
         mbar_arrive(&ctrl->work);
       }
-    } else if (warp >= 4) {
-      // rescale / epilogue warpgroup: thread h owns O row h (TMEM lane h)
-      const int h = tid - 128;
-      const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    } else if (warp >= 4 && warp < 12) {
+      // rescale / epilogue: O row h, columns [256*half, 256*half + 256)
+      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16) + half * 256;
       uint32_t wphase = 0;
       while (true) {
         if (!warp_wait(&ctrl->work, wphase, p.status, abort_flag)) break;
@@ -510,7 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           const bool need = __any_sync(0xffffffffu, alpha != 1.f);
           if (need) {
 #pragma unroll 1
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8; ++c) {
               uint32_t r[32];
               tmem_ld32(lane_base + c * 32, r);
               tmem_ld_wait();
@@ -526,9 +661,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           const float inv = l > 0.f ? 1.f / l : 0.f;
           const float lse = l > 0.f ? (mrow + __log2f(l)) * kLn2 : -INFINITY;
           if (pc.slot < 0) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o_lat + ((size_t)pc.item * kH + h) * kDC);
+            uint4* dst = reinterpret_cast<uint4*>(p.o_lat + ((size_t)pc.item * kH + h) * kDC + half * 256);
 #pragma unroll 1
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8; ++c) {
               uint32_t r[32];
               tmem_ld32(lane_base + c * 32, r);
               tmem_ld_wait();
@@ -542,11 +677,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 dst[c * 4 + i] = v;
               }
             }
-            if (p.lse_out) p.lse_out[(size_t)pc.item * kH + h] = lse;
+            if (p.lse_out && half == 0) p.lse_out[(size_t)pc.item * kH + h] = lse;
           } else {
-            float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)pc.slot * kH + h) * kDC);
+            float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)pc.slot * kH + h) * kDC + half * 256);
 #pragma unroll 1
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8; ++c) {
               uint32_t r[32];
               tmem_ld32(lane_base + c * 32, r);
               tmem_ld_wait();
@@ -555,7 +690,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 dst[c * 8 + i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
                                              __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
             }
-            p.part_lse[(size_t)pc.slot * kH + h] = lse;
+            if (half == 0) p.part_lse[(size_t)pc.slot * kH + h] = lse;
           }
         }
         tc_fence_before();
@@ -654,7 +789,7 @@ int cluster_count(int device, int sm_count) {
   if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * n, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -719,11 +854,18 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   int2* cluster_range = reinterpret_cast<int2*>(ws + w.cluster_range);
   Piece* pieces = reinterpret_cast<Piece*>(ws + w.pieces);
 
-  CUtensorMap map;
-  const cuuint64_t dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kBlk, (cuuint64_t)cache.num_blocks};
-  const cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, (cuuint64_t)kBlk * kRow * 2};
-  const cuuint32_t box[3] = {64, 64, 1}, estride[3] = {1, 1, 1};
-  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, cache.pool, dims, strides, box, estride,
+  // The pool viewed as [block][64-element chunk][token][element]; a box of 5 or 4 chunks lands
+  // as [chunk][token][128 B] with the 128-byte swizzle the MMA descriptors expect.
+  CUtensorMap map5, map4;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)kBlk, (cuuint64_t)kChunks, (cuuint64_t)cache.num_blocks};
+  const cuuint64_t strides[3] = {(cuuint64_t)kRow * 2, 128, (cuuint64_t)kBlk * kRow * 2};
+  const cuuint32_t box5[4] = {64, (cuuint32_t)kBlk, (cuuint32_t)kKSplit, 1};
+  const cuuint32_t box4[4] = {64, (cuuint32_t)kBlk, 4, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  if (encode(&map5, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache.pool, dims, strides, box5, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      encode(&map4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache.pool, dims, strides, box4, estride,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -751,7 +893,7 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   prm.status = ctx.status;
   e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<<<2 * C, 256, kSmemBytes, ctx.stream>>>(map, prm);
+  decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, ctx.stream>>>(map5, map4, prm);
   count_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -763,3 +905,4 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
 }
 
 }  // namespace mla
+
