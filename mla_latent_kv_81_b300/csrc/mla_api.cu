@@ -19,6 +19,33 @@ static std::atomic<uint64_t> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 namespace {
+struct SmemLimit {
+  const void* kernel;
+  int device;
+  int bytes;
+};
+std::mutex g_smem_mutex;
+SmemLimit g_smem_limits[256];
+int g_smem_count = 0;
+}  // namespace
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes, int device) {
+  std::lock_guard<std::mutex> lock(g_smem_mutex);
+  for (int i = 0; i < g_smem_count; ++i) {
+    SmemLimit& l = g_smem_limits[i];
+    if (l.kernel == kernel && l.device == device) {
+      if (l.bytes >= bytes) return cudaSuccess;
+      const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) l.bytes = bytes;
+      return e;
+    }
+  }
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && g_smem_count < 256) g_smem_limits[g_smem_count++] = {kernel, device, bytes};
+  return e;
+}
+
+namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;

@@ -27,6 +27,10 @@ template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __f
 // Host-side count of kernel launches (see mla_kernel_launches()).
 void count_launch(int n = 1);
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on `device`, calling the runtime only when
+// the limit grows (so that launches made while a stream is being captured into a graph do not).
+cudaError_t ensure_smem_limit(const void* kernel, int bytes, int device);
+
 __device__ __forceinline__ void flag_error(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
 
 // Resolved logical -> physical row of the paged cache, or -1 (and a flag) when

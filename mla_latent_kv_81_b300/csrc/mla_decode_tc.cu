@@ -786,7 +786,7 @@ int cluster_count(int device, int sm_count) {
     if (device >= 0 && device < 64 && g_clusters[device] > 0) return g_clusters[device];
   }
   int n = sm_count / 2;
-  if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) == cudaSuccess) {
+  if (ensure_smem_limit((const void*)decode_tc_kernel, kSmemBytes, device) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * n, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -891,7 +891,7 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   prm.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
   prm.scale_log2 = scale * kLog2e;
   prm.status = ctx.status;
-  e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = ensure_smem_limit((const void*)decode_tc_kernel, kSmemBytes, ctx.device);
   if (e != cudaSuccess) return e;
   decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, ctx.stream>>>(map5, map4, prm);
   count_launch();

@@ -322,14 +322,16 @@ cudaError_t simt_decode(const Ctx& c, int dtype, const void* q, const mla_paged_
   const float scale_log2 = scale * kLog2e;
   if (dtype == MLA_BF16) {
     auto k = simt_decode_kernel<bf16>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t ea = ensure_smem_limit((const void*)k, (int)smem, c.device);
+    if (ea != cudaSuccess) return ea;
     k<<<grid, 128, smem, c.stream>>>((const bf16*)q, (const bf16*)cache.pool, cache.block_table,
                                      cache.max_blocks_per_seq, cache.num_blocks, block_size, kv_len, n_q, H, d_c, d_r,
                                      scale_log2, splits, tokens_per_split, part_o, part_lse, (bf16*)o_lat, lse_out,
                                      c.status);
   } else {
     auto k = simt_decode_kernel<float>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t ea = ensure_smem_limit((const void*)k, (int)smem, c.device);
+    if (ea != cudaSuccess) return ea;
     k<<<grid, 128, smem, c.stream>>>((const float*)q, (const float*)cache.pool, cache.block_table,
                                      cache.max_blocks_per_seq, cache.num_blocks, block_size, kv_len, n_q, H, d_c, d_r,
                                      scale_log2, splits, tokens_per_split, part_o, part_lse, (float*)o_lat, lse_out,
