@@ -185,6 +185,29 @@ mla_status mla_output_project(const mla_config* cfg, const void* o_lat, const vo
  * *flags (if not NULL) receives the raw bit set (bit 0 index, bit 1 timeout). */
 mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags);
 
+/* mla_compress_append without a workspace argument.  No counterpart on the pages:
+ * an interface for callers that cannot allocate device memory, for example code
+ * that runs where every device allocation is owned by a fixed pool or arena
+ * set up at start-up (inference servers, embedded runtimes, other languages'
+ * runtimes holding only raw device pointers), or that may not call cudaMalloc
+ * on the decode path because it would synchronise the device.
+ * Same operation, arguments and error behaviour as mla_compress_append, except:
+ *   - the fp32 scratch lives in one fixed 16 MiB array inside the library
+ *     (every GPU that loads the library holds it until the process exits);
+ *     a call whose scratch would exceed it (mla_compress_workspace_bytes(cfg, T)
+ *     > 16 MiB) returns MLA_ERR_WORKSPACE without touching the GPU; with the
+ *     DeepSeek-V2 shape every call of up to 1024 tokens fits;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before capturing a stream;
+ *   - all calls on a device share the array and it keeps the last call's
+ *     contents (nothing in it has to start at zero: each call writes every
+ *     element it reads), so calls that overlap on the GPU (e.g. on two
+ *     streams at once) race; order them on one stream.
+ * The function allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+mla_status mla_compress_append_noalloc(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
+                                       const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
+                                       const mla_paged_cache* cache, int T, mla_stream_t stream);
+
 /* Number of kernels this library has launched in this process (all devices).
  * For accounting in benchmarks; no counterpart on the pages. */
 uint64_t mla_kernel_launches(void);

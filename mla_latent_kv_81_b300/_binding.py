@@ -61,6 +61,7 @@ def _load():
         "mla_get_device_status": (I, [VP, P(ctypes.c_uint32)]),
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_kernel_launches": (ctypes.c_uint64, []),
+        "mla_compress_append_noalloc": (I, [cfgp, VP, VP, VP, VP, VP, ropep, cachep, I, VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -72,7 +73,8 @@ lib = _load()
 EXPORTED = ("mla_cache_bytes_per_token", "mla_rope_table_create", "mla_compress_workspace_bytes",
             "mla_compress_append", "mla_absorb_workspace_bytes", "mla_absorb_query",
             "mla_decode_workspace_bytes", "mla_decode_attention", "mla_output_workspace_bytes",
-            "mla_output_project", "mla_get_device_status", "mla_status_string", "mla_kernel_launches")
+            "mla_output_project", "mla_get_device_status", "mla_status_string", "mla_kernel_launches",
+            "mla_compress_append_noalloc")
 
 
 # ------------------------------------------------------------------ marshalling helpers
@@ -137,6 +139,15 @@ def mla_compress_append(cfg, x, W_DKV, W_KR, seq_idx, pos, rope: mla_rope_table,
            lib.mla_compress_append(ctypes.byref(cfg), _ptr(x), _ptr(W_DKV), _ptr(W_KR), _ptr(seq_idx), _ptr(pos),
                                    ctypes.byref(rope), ctypes.byref(cache), T, _ptr(ws), ws.numel(),
                                    _stream(stream)))
+
+
+def mla_compress_append_noalloc(cfg, x, W_DKV, W_KR, seq_idx, pos, rope: mla_rope_table, cache: mla_paged_cache,
+                                stream=None):
+    """mla_compress_append with its scratch in the library's fixed device array (no workspace)."""
+    _check("mla_compress_append_noalloc",
+           lib.mla_compress_append_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(W_DKV), _ptr(W_KR), _ptr(seq_idx),
+                                           _ptr(pos), ctypes.byref(rope), ctypes.byref(cache), x.shape[0],
+                                           _stream(stream)))
 
 
 def mla_absorb_workspace_bytes(cfg, N):
