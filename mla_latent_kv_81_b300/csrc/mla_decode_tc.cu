@@ -9,17 +9,21 @@
 //
 // A full fp32 accumulator O (128 heads x 512) fills all of one SM's tensor
 // memory, so each unit of work runs on a cluster of two CTAs:
-//   * the score CTA (rank 0) keeps the absorbed query Q [128 x 576] in TMEM,
-//     streams [64 tokens x 576] tiles with TMA, computes S = Q K^T (A from
-//     TMEM), and runs the online softmax with two threads per head row; it
-//     pushes bf16 P (and the per-row rescale factor) into the value CTA's
-//     shared memory with st.async;
-//   * the value CTA (rank 1) streams the [64 x 512] latent part of the same
-//     tiles and accumulates O += P V in all 512 TMEM columns; two warpgroups
-//     rescale O when the running maximum jumps (rarely) and write the result.
-// The cached tokens of all queries are cut into equal tile ranges, one per
-// cluster (split-KV); ranges that cover part of a query write fp32 partials
-// that a second kernel merges by log-sum-exp.
+//   * the score CTA (rank 0) keeps the latent part of the absorbed query in
+//     TMEM and its positional part in shared memory, streams the cache in
+//     128-token tiles (two blocks) through a ring of 16 KB chunk slots with
+//     TMA, computes S = Q K^T with N = 128 MMAs (the tensor core runs N = 64
+//     at about 60% of its rate), and runs the online softmax with two threads
+//     per head row (one per 64-token half); each half is one unit of bf16 P
+//     that the softmax threads push, with the per-row rescale factor, into the
+//     value CTA's shared memory with st.async;
+//   * the value CTA (rank 1) streams the [64 x 512] latent part of every block
+//     as two 32 KB halves and accumulates O += P V in all 512 TMEM columns;
+//     two warpgroups rescale O when the running maximum jumps (rarely) and
+//     write the result.
+// The cached tokens of all queries are cut into equal ranges of 128-token
+// tiles, one per cluster (split-KV); ranges that cover part of a query write
+// fp32 partials that a second kernel merges by log-sum-exp.
 #include <math.h>
 
 #include <mutex>
@@ -32,47 +36,49 @@ namespace {
 using namespace sm100;
 
 constexpr int kH = 128, kDC = 512, kDR = 64, kRow = 576, kBlk = 64;
-constexpr int kThreads = 512;  // warps 0-3: TMA, MMA, TMEM, spare; 4-11: two warpgroups; 12-15: P sender
-constexpr int kBoxBytes = 64 * 64 * 2;             // one swizzled [64 tokens x 64 elements] chunk
+constexpr int kTile = 2 * kBlk;                     // tokens per score tile: N of the score MMAs
+constexpr int kThreads = 384;                       // warps 0-3: TMA, MMA, TMEM, spare; 4-11: two warpgroups
+constexpr int kBoxBytes = 64 * 64 * 2;              // one swizzled [64 tokens x 64 elements] box
 constexpr int kChunks = kRow / 64;                  // 9 chunks per cached row: 8 latent + 1 positional
-constexpr int kKStageBytes = kChunks * kBoxBytes;   // score CTA: whole rows (73,728 B)
-constexpr int kVStageBytes = 8 * kBoxBytes;         // value CTA: latent part (65,536 B)
-constexpr int kKStages = 3;
-constexpr int kKSplit = 5;                          // a score stage loads and frees as chunks 0-4 and chunks 5-8
-constexpr int kVStages = 2;
-constexpr int kPSlots = 3;
-constexpr int kSlotBytes = 18432;                   // P 16 KB | alpha | l (cols 0-31) | l (cols 32-63) | m
+constexpr int kSlotK = 2 * kBoxBytes;               // score ring slot: one chunk of a 128-token tile
+constexpr int kRing = 12;
+constexpr int kSlotV = 4 * kBoxBytes;               // value ring slot: four latent chunks of one block
+constexpr int kVRing = 5;
+constexpr int kPSlots = 3;                          // P units (64 tokens) in flight to the value CTA
+constexpr int kSlotBytes = 18432;                   // P 16 KB | alpha | l (tokens 0-63) | l (64-127) | m
 constexpr int kSlotAlpha = 16384, kSlotL0 = 16896, kSlotL1 = 17408, kSlotM = 17920;
 constexpr int kCtrlBytes = 4096;
-constexpr int kOffStages = kCtrlBytes;                               // both roles
-constexpr int kOffSlots = kOffStages + kVStages * kVStageBytes;     // value CTA
-constexpr int kSmemScore = kOffStages + kKStages * kKStageBytes;
+constexpr int kOffQR = kCtrlBytes;                  // score CTA: positional part of Q, [128 rows x 128 B]
+constexpr int kOffRing = kOffQR + kH * 128;
+constexpr int kOffV = kCtrlBytes;                   // value CTA
+constexpr int kOffSlots = kOffV + kVRing * kSlotV;
+constexpr int kSmemScore = kOffRing + kRing * kSlotK;
 constexpr int kSmemValue = kOffSlots + kPSlots * kSlotBytes;
 constexpr int kSmemBytes = (kSmemScore > kSmemValue ? kSmemScore : kSmemValue) + 1024;  // + alignment slack
-constexpr uint32_t kTxTile = 16384 + 512;
-constexpr uint32_t kTxLast = kTxTile + 1536;
-// score CTA TMEM columns: S buffers at 0 and 64, Q at 128..415, two staged P tiles at 416 and 448
-// (64 bf16 per row packed in 32 columns), per-row alpha / l (two halves) / m of each staged tile at 480 + 4*slot
-constexpr int kSCol = 0, kQCol = 128, kPStageCol = 416, kPExtraCol = 480;
+static_assert(kOffRing % 1024 == 0 && kOffSlots % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle alignment");
+static_assert(kSmemBytes <= 232448, "shared memory");
+constexpr uint32_t kTxUnit = 16384 + 512;
+constexpr uint32_t kTxLast = kTxUnit + 1536;
+// score CTA TMEM columns: S buffers at 0 and 128, latent Q at 256..511 (64 bf16 per 32 columns)
+constexpr int kSCol = 0, kQCol = 256;
 constexpr float kRescaleThreshold = 8.0f;            // log2 units: rescale O only when the max grows by 2^8
 
 enum : int { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
 
 struct Piece {
   int item;     // b * n_q + j
-  int t_begin;  // first token (multiple of 64)
+  int t_begin;  // first token (multiple of 128)
   int t_end;    // one past the last token
   int slot;     // partial slot, or -1 when the piece is the whole query
 };
 
 struct Ctrl {
-  uint64_t k_full[kKStages][2], k_empty[kKStages][2];   // [stage][chunks 0-4 | chunks 5-8]
+  uint64_t k_full[kRing], k_empty[kRing];
   uint64_t s_full[2], s_empty[2];
   uint64_t q_ready;
   uint64_t xch[2];
-  uint64_t p_staged[2], p_free[2];
   uint64_t p_empty[kPSlots];
-  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t v_full[kVRing], v_empty[kVRing];
   uint64_t p_full[kPSlots];
   uint64_t mma_idle, work, done;
   uint32_t tmem_base;
@@ -80,7 +86,7 @@ struct Ctrl {
   int cmd, cmd_slot, cmd_piece;
   float l_buf[kH];
   float m_buf[kH];
-  float half_max[2][2][kH];   // [tile parity][column half][row]
+  float half_max[2][2][kH];   // [tile parity][token half][row]
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 
@@ -101,14 +107,15 @@ struct Params {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Walks the tiles of a cluster's pieces in order.
+// Walks a cluster's pieces in steps of `step` tokens.
 struct TileCursor {
-  int pi, end, t, t_end, b;
-  __device__ void start(const Piece* pieces, int first, int last, int n_q) {
+  int pi, end, t, t_end, b, step;
+  __device__ void start(const Piece* pieces, int first, int last, int n_q, int step_) {
     pi = first - 1;
     end = last;
     t = t_end = 0;
     b = 0;
+    step = step_;
     next_piece(pieces, n_q);
   }
   __device__ void next_piece(const Piece* pieces, int n_q) {
@@ -124,20 +131,23 @@ struct TileCursor {
   }
   __device__ bool valid() const { return pi < end; }
   __device__ void advance(const Piece* pieces, int n_q) {
-    t += kBlk;
+    t += step;
     if (t >= t_end) next_piece(pieces, n_q);
   }
 };
 
-constexpr int kLookahead = 4;   // block-table entries read this many tiles before their loads
+// Block-table entries are loaded this many steps before their TMA loads and checked only when used,
+// so the latency of the table read never sits in front of a load.
+constexpr int kLookahead = 4;
 
-// Physical block of the cursor's tile (0 and a flag when the table entry is out of range), or -1 past the end.
-__device__ __forceinline__ int block_of(const TileCursor& c, const int32_t* table, int max_blocks, int num_blocks,
-                                        uint32_t* status, bool flag) {
-  if (!c.valid()) return -1;
-  int blk = __ldg(table + (long long)c.b * max_blocks + c.t / kBlk);
-  if (blk < 0 || blk >= num_blocks) {
-    if (flag) flag_error(status, kFlagIndex);
+// Table entry `idx` of sequence b, loaded but not yet checked.
+__device__ __forceinline__ int table_raw(const Params& p, int b, int idx) {
+  return __ldg(p.table + (long long)b * p.max_blocks + idx);
+}
+// A loaded entry as a physical block (0 and a flag when it is out of range).
+__device__ __forceinline__ int checked_block(const Params& p, int blk, bool flag) {
+  if (blk < 0 || blk >= p.num_blocks) {
+    if (flag) flag_error(p.status, kFlagIndex);
     blk = 0;
   }
   return blk;
@@ -151,7 +161,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // ------------------------------------------------------------------ planner
-// One CTA of 1024 threads.  Cuts the visible tiles of all queries into C
+// One CTA of 1024 threads.  Cuts the visible 128-token tiles of all queries into C
 // equal contiguous ranges (cluster c gets global tiles [c*T/C, (c+1)*T/C))
 // and lists the resulting pieces in global tile order.
 constexpr int kPlanThreads = 1024;
@@ -206,7 +216,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* kv_le
   int carry = 0;
   for (int base = 0; base < items; base += kPlanThreads) {
     const int i = base + threadIdx.x;
-    const int tiles = i < items ? ceil_div(visible_tokens(kv_len, i, n_q, cap, status, true), kBlk) : 0;
+    const int tiles = i < items ? ceil_div(visible_tokens(kv_len, i, n_q, cap, status, true), kTile) : 0;
     int tot;
     const int ex = block_scan_excl(tiles, sh, tot);
     if (i < items) prefix[i] = carry + ex;
@@ -251,8 +261,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* kv_le
       const long long a = lo > P0 ? lo : P0, e = hi < P1 ? hi : P1;
       Piece pc;
       pc.item = i;
-      pc.t_begin = (int)(a - P0) * kBlk;
-      pc.t_end = (int)(e - P0) * kBlk;
+      pc.t_begin = (int)(a - P0) * kTile;
+      pc.t_end = (int)(e - P0) * kTile;
       if (pc.t_end > vis) pc.t_end = vis;
       pc.slot = r.y > 1 ? slot_off[i] + k : -1;
       const int idx = r.x + k;
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* kv_le
 
 // ------------------------------------------------------------------ attention kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap map5, const __grid_constant__ CUtensorMap map4, Params p) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap map1, const __grid_constant__ CUtensorMap map4, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
@@ -275,18 +285,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &ctrl->abort_flag;
 
   if (tid == 0) {
-    for (int i = 0; i < kKStages; ++i)
-      for (int j = 0; j < 2; ++j) { mbar_init(&ctrl->k_full[i][j], 1); mbar_init(&ctrl->k_empty[i][j], 1); }
+    for (int i = 0; i < kRing; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->s_full[i], 1);
       mbar_init(&ctrl->s_empty[i], 256);
       mbar_init(&ctrl->xch[i], 256);
-      mbar_init(&ctrl->p_staged[i], 256);
-      mbar_init(&ctrl->p_free[i], 128);
     }
     mbar_init(&ctrl->q_ready, 256);
     for (int i = 0; i < kPSlots; ++i) { mbar_init(&ctrl->p_empty[i], 1); mbar_init(&ctrl->p_full[i], 1); }
-    for (int i = 0; i < kVStages; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
+    for (int i = 0; i < kVRing; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
     mbar_init(&ctrl->mma_idle, 1);
     mbar_init(&ctrl->work, 1);
     mbar_init(&ctrl->done, 256);
@@ -298,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&map5);
+    prefetch_tmap(&map1);
     prefetch_tmap(&map4);
   }
   tc_fence_before();
@@ -308,7 +315,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctrl->tmem_base;
   const int2 range = p.cluster_range[cid];
   const uint32_t smem_base = smem_u32(smem);
-  // warpgroup lanes: warps 4..11, quarter q = TMEM lane group, half = which 32 columns / 256 O columns
+  // warpgroup lanes: warps 4..11, quarter q4 = TMEM lane group, half = which 64 tokens / 256 O columns
   const int q4 = warp & 3, half = (warp - 4) >> 2;
   const int h = q4 * 32 + lane;
 
@@ -316,85 +323,103 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // =========================== score CTA ===========================
     if (warp == 0) {
       if (lane == 0) {
-        // block-table entries are read kLookahead tiles ahead so their latency overlaps the stage waits
-        int stage = 0;
+        // ring slot = one 64-element chunk of a 128-token tile: chunk c of the tile's first block at +0,
+        // of its second block at +8 KB (absent in a one-block tail tile)
+        int r = 0;
         uint32_t phase = 0;
         TileCursor ahead;
-        ahead.start(p.pieces, range.x, range.y, p.n_q);
-        int nb[kLookahead];
+        ahead.start(p.pieces, range.x, range.y, p.n_q, kTile);
+        // raw entries of the next kLookahead tiles; bit u of `live` / `two`: tile u exists / has a second block
+        int raw0[kLookahead], raw1[kLookahead];
+        uint32_t live = 0, two = 0;
 #pragma unroll
-        for (int i = 0; i < kLookahead; ++i) {
-          nb[i] = block_of(ahead, p.table, p.max_blocks, p.num_blocks, p.status, true);
-          if (ahead.valid()) ahead.advance(p.pieces, p.n_q);
+        for (int u = 0; u < kLookahead; ++u) {
+          raw0[u] = raw1[u] = 0;
+          if (ahead.valid()) {
+            live |= 1u << u;
+            raw0[u] = table_raw(p, ahead.b, ahead.t / kBlk);
+            if (ahead.t + kBlk < ahead.t_end) { two |= 1u << u; raw1[u] = table_raw(p, ahead.b, ahead.t / kBlk + 1); }
+            ahead.advance(p.pieces, p.n_q);
+          }
         }
-        bool more = nb[0] >= 0;
-        while (more) {
+        while (live & 1u) {
 #pragma unroll
           for (int u = 0; u < kLookahead; ++u) {
-            const int blk = nb[u];
-            if (blk < 0) { more = false; break; }
-            nb[u] = block_of(ahead, p.table, p.max_blocks, p.num_blocks, p.status, true);
-            if (ahead.valid()) ahead.advance(p.pieces, p.n_q);
-            uint8_t* dst = smem + kOffStages + stage * kKStageBytes;
-            if (!mbar_wait(&ctrl->k_empty[stage][0], phase ^ 1, p.status, abort_flag)) goto score_done;
-            mbar_arrive_expect_tx(&ctrl->k_full[stage][0], kKSplit * kBoxBytes);
-            tma_load_4d(dst, &map5, &ctrl->k_full[stage][0], 0, 0, 0, blk);
-            if (!mbar_wait(&ctrl->k_empty[stage][1], phase ^ 1, p.status, abort_flag)) goto score_done;
-            mbar_arrive_expect_tx(&ctrl->k_full[stage][1], (kChunks - kKSplit) * kBoxBytes);
-            tma_load_4d(dst + kKSplit * kBoxBytes, &map4, &ctrl->k_full[stage][1], 0, 0, kKSplit, blk);
-            if (++stage == kKStages) { stage = 0; phase ^= 1; }
+            if (!(live & (1u << u))) break;
+            const int b0 = checked_block(p, raw0[u], true);
+            const int b1 = (two & (1u << u)) ? checked_block(p, raw1[u], true) : -1;
+            live &= ~(1u << u);
+            two &= ~(1u << u);
+            if (ahead.valid()) {   // refill this entry with the tile kLookahead steps ahead
+              live |= 1u << u;
+              raw0[u] = table_raw(p, ahead.b, ahead.t / kBlk);
+              if (ahead.t + kBlk < ahead.t_end) { two |= 1u << u; raw1[u] = table_raw(p, ahead.b, ahead.t / kBlk + 1); }
+              ahead.advance(p.pieces, p.n_q);
+            }
+#pragma unroll 1
+            for (int c = 0; c < kChunks; ++c) {
+              if (!mbar_wait(&ctrl->k_empty[r], phase ^ 1, p.status, abort_flag)) goto score_done;
+              uint8_t* dst = smem + kOffRing + r * kSlotK;
+              mbar_arrive_expect_tx(&ctrl->k_full[r], b1 >= 0 ? 2 * kBoxBytes : kBoxBytes);
+              tma_load_4d(dst, &map1, &ctrl->k_full[r], 0, 0, c, b0);
+              if (b1 >= 0) tma_load_4d(dst + kBoxBytes, &map1, &ctrl->k_full[r], 0, 0, c, b1);
+              if (++r == kRing) { r = 0; phase ^= 1; }
+            }
           }
         }
       }
     } else if (warp == 1) {
       if (lane == 0) {
-        const uint32_t idesc = idesc_bf16(128, 64, false, false);
-        const uint64_t kdesc0 = desc_sw128(smem_base + kOffStages, 16, 1024);
-        int stage = 0, sbuf = 0;
+        // S[128 heads x 128 tokens] = Q K^T over 9 chunks of 4 K-steps; latent chunks take A from TMEM,
+        // the positional chunk from shared memory; every chunk's slot is released when its MMAs complete
+        const uint32_t idesc = idesc_bf16(128, kTile, false, false);
+        const uint64_t ring0 = desc_sw128(smem_base + kOffRing, 16, 1024);
+        const uint64_t qr0 = desc_sw128(smem_base + kOffQR, 16, 1024);
+        int r = 0, sbuf = 0;
         uint32_t kphase = 0, sphase = 0, qphase = 0;
         for (int pi = range.x; pi < range.y; ++pi) {
           const Piece pc = p.pieces[pi];
           if (pc.t_end <= pc.t_begin) continue;
           if (!mbar_wait(&ctrl->q_ready, qphase, p.status, abort_flag)) goto score_done;
           qphase ^= 1;
-          for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
+          for (int t = pc.t_begin; t < pc.t_end; t += kTile) {
             if (!mbar_wait(&ctrl->s_empty[sbuf], sphase ^ 1, p.status, abort_flag)) goto score_done;
-            const uint64_t kd = kdesc0 + (uint64_t)(stage * (kKStageBytes >> 4));
-            const uint32_t d = tmem + kSCol + sbuf * 64;
-            // 36 K-steps of 16: chunk s/4 (8 KB apart), 32 B within the 128-B swizzled row;
-            // each half of the stage is released as soon as its MMAs complete
-            if (!mbar_wait(&ctrl->k_full[stage][0], kphase, p.status, abort_flag)) goto score_done;
-            tc_fence_after();
+            const uint32_t d = tmem + kSCol + sbuf * kTile;
 #pragma unroll
-            for (int s = 0; s < 4 * kKSplit; ++s)
-              mma_ts(d, tmem + kQCol + s * 8, kd + (uint64_t)((s >> 2) * (kBoxBytes >> 4) + (s & 3) * 2), idesc,
-                     s > 0 ? 1u : 0u);
-            mma_commit(&ctrl->k_empty[stage][0]);
-            if (!mbar_wait(&ctrl->k_full[stage][1], kphase, p.status, abort_flag)) goto score_done;
-            tc_fence_after();
+            for (int c = 0; c < kChunks; ++c) {
+              if (!mbar_wait(&ctrl->k_full[r], kphase, p.status, abort_flag)) goto score_done;
+              tc_fence_after();
+              const uint64_t kd = ring0 + (uint64_t)(r * (kSlotK >> 4));
 #pragma unroll
-            for (int s = 4 * kKSplit; s < kRow / 16; ++s)
-              mma_ts(d, tmem + kQCol + s * 8, kd + (uint64_t)((s >> 2) * (kBoxBytes >> 4) + (s & 3) * 2), idesc, 1u);
-            mma_commit(&ctrl->k_empty[stage][1]);
+              for (int k = 0; k < 4; ++k) {
+                if (c < kChunks - 1)
+                  mma_ts(d, tmem + kQCol + c * 32 + k * 8, kd + (uint64_t)(k * 2), idesc, (c | k) ? 1u : 0u);
+                else
+                  mma_ss(d, qr0 + (uint64_t)(k * 2), kd + (uint64_t)(k * 2), idesc, 1u);
+              }
+              mma_commit(&ctrl->k_empty[r]);
+              if (++r == kRing) { r = 0; kphase ^= 1; }
+            }
             mma_commit(&ctrl->s_full[sbuf]);
-            if (++stage == kKStages) { stage = 0; kphase ^= 1; }
             if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
           }
         }
       }
     } else if (warp >= 4 && warp < 12) {
-      // softmax: head row h, columns [32*half, 32*half + 32) of each tile
+      // softmax: head row h, tokens [64*half, 64*half + 64) of each tile, which form one unit of P
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-      int sbuf = 0, tile = 0;
+      const uint32_t peer_slots = mapa(smem_base + kOffSlots, 1);
+      int sbuf = 0, tile = 0, unit = 0;
       uint32_t sphase = 0;
       for (int pi = range.x; pi < range.y; ++pi) {
         const Piece pc = p.pieces[pi];
         if (pc.t_end <= pc.t_begin) continue;
         {
-          // absorbed query row h -> TMEM columns [kQCol, kQCol + 288); chunks 0-4 / 5-8 per half
+          // absorbed query row h: latent chunks 4*half .. 4*half+3 -> TMEM; the positional part -> the
+          // swizzled shared-memory rows the MMA reads as A
           const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)pc.item * kH + h) * kRow);
 #pragma unroll 1
-          for (int c = half * 5; c < (half ? 9 : 5); ++c) {
+          for (int c = 4 * half; c < 4 * half + 4; ++c) {
             uint32_t r[32];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -403,28 +428,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tmem_st32(lane_base + kQCol + c * 32, r);
           }
+          if (half == 1) {
+            uint8_t* qr = smem + kOffQR + h * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(qr + ((u ^ (h & 7)) << 4)) = __ldg(src + 64 + u);
+            fence_proxy_async_smem();
+          }
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&ctrl->q_ready);
         }
         float m = -INFINITY, lpart = 0.f;
-        for (int t = pc.t_begin; t < pc.t_end; t += kBlk, ++tile) {
-          const int valid = min(kBlk, pc.t_end - t) - half * 32;   // valid columns in this half (may be <= 0)
-          const bool first = (t == pc.t_begin), last = (t + kBlk >= pc.t_end);
+        for (int t = pc.t_begin; t < pc.t_end; t += kTile, ++tile) {
+          const int ntok = min(kTile, pc.t_end - t);
+          const int nunits = ntok > kBlk ? 2 : 1;
+          const int valid = ntok - half * kBlk;   // valid columns of this half (may be <= 0)
+          const bool first = (t == pc.t_begin), last = (t + kTile >= pc.t_end);
           if (!warp_wait(&ctrl->s_full[sbuf], sphase, p.status, abort_flag)) goto score_done;
           tc_fence_after();
-          uint32_t sr[32];
-          tmem_ld32(lane_base + kSCol + sbuf * 64 + half * 32, sr);
+          uint32_t sa[32], sb[32];   // columns 0-31 and 32-63 of this half
+          tmem_ld32(lane_base + kSCol + sbuf * kTile + half * kBlk, sa);
+          tmem_ld32(lane_base + kSCol + sbuf * kTile + half * kBlk + 32, sb);
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&ctrl->s_empty[sbuf]);
           if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
-          float x[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = i < valid ? __uint_as_float(sr[i]) * p.scale_log2 : -INFINITY;
+          for (int i = 0; i < 32; ++i) {
+            sa[i] = __float_as_uint(i < valid ? __uint_as_float(sa[i]) * p.scale_log2 : -INFINITY);
+            sb[i] = __float_as_uint(i + 32 < valid ? __uint_as_float(sb[i]) * p.scale_log2 : -INFINITY);
+          }
           float mx8[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(fmaxf(x[i], x[i + 8]), fmaxf(x[i + 16], x[i + 24]));
+          for (int i = 0; i < 8; ++i)
+            mx8[i] = fmaxf(fmaxf(fmaxf(__uint_as_float(sa[i]), __uint_as_float(sa[i + 8])),
+                                 fmaxf(__uint_as_float(sa[i + 16]), __uint_as_float(sa[i + 24]))),
+                           fmaxf(fmaxf(__uint_as_float(sb[i]), __uint_as_float(sb[i + 8])),
+                                 fmaxf(__uint_as_float(sb[i + 16]), __uint_as_float(sb[i + 24]))));
           const float hmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
           // exchange the half-row maxima with the partner thread of the other warpgroup
@@ -440,67 +480,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             lpart *= alpha;
             m = mx;
           }
-          uint32_t pk[16];
+          uint32_t pk[32];
           float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(x[2 * i] - m), p1 = ex2(x[2 * i + 1] - m);
-            ps[i & 3] += p0 + p1;
+            const float p0 = ex2(__uint_as_float(sa[2 * i]) - m), p1 = ex2(__uint_as_float(sa[2 * i + 1]) - m);
+            const float p2 = ex2(__uint_as_float(sb[2 * i]) - m), p3 = ex2(__uint_as_float(sb[2 * i + 1]) - m);
+            ps[i & 3] += (p0 + p1) + (p2 + p3);
             pk[i] = pack_bf16x2(p0, p1);
+            pk[16 + i] = pack_bf16x2(p2, p3);
           }
           lpart += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-          // stage P and the row statistics in TMEM; the sender warpgroup pushes them to the value CTA
-          const int st = tile & 1;
-          if (!warp_wait(&ctrl->p_free[st], ((tile >> 1) & 1) ^ 1, p.status, abort_flag)) goto score_done;
-          tc_fence_after();
-          tmem_st16(lane_base + kPStageCol + st * 32 + half * 16, pk);
-          if (half == 0) {
-            tmem_st1(lane_base + kPExtraCol + st * 4 + 0, __float_as_uint(alpha));
-            tmem_st1(lane_base + kPExtraCol + st * 4 + 1, __float_as_uint(lpart));
-            tmem_st1(lane_base + kPExtraCol + st * 4 + 3, __float_as_uint(m));
-          } else {
-            tmem_st1(lane_base + kPExtraCol + st * 4 + 2, __float_as_uint(lpart));
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&ctrl->p_staged[st]);
-        }
-      }
-    } else if (warp >= 12) {
-      // P sender: TMEM-staged tiles -> value CTA slots (st.async), row h = lane of this warp's quarter
-      const int hs = (warp & 3) * 32 + lane;
-      const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      const uint32_t peer_slots = mapa(smem_base + kOffSlots, 1);
-      int pslot = 0, tile = 0;
-      uint32_t pphase = 0;
-      for (int pi = range.x; pi < range.y; ++pi) {
-        const Piece pc = p.pieces[pi];
-        if (pc.t_end <= pc.t_begin) continue;
-        for (int t = pc.t_begin; t < pc.t_end; t += kBlk, ++tile) {
-          const bool last = (t + kBlk >= pc.t_end);
-          const int st = tile & 1;
-          if (!warp_wait(&ctrl->p_staged[st], (tile >> 1) & 1, p.status, abort_flag)) goto score_done;
-          tc_fence_after();
-          uint32_t pk[32], ex[4];
-          tmem_ld32(lane_base + kPStageCol + st * 32, pk);
-          tmem_ld4(lane_base + kPExtraCol + st * 4, ex);
-          tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(&ctrl->p_free[st]);
-          if (!warp_wait(&ctrl->p_empty[pslot], pphase ^ 1, p.status, abort_flag)) goto score_done;
-          const uint32_t slot = peer_slots + pslot * kSlotBytes;
-          const uint32_t rbar = mapa(smem_u32(&ctrl->p_full[pslot]), 1);
+          // this half's unit of P (and its rescale factor) -> the value CTA's slot
+          if (half < nunits) {
+            const int u = unit + half, slot = u % kPSlots;
+            if (!warp_wait(&ctrl->p_empty[slot], ((u / kPSlots) & 1) ^ 1, p.status, abort_flag)) goto score_done;
+            const uint32_t sl = peer_slots + slot * kSlotBytes;
+            const uint32_t rbar = mapa(smem_u32(&ctrl->p_full[slot]), 1);
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_async_v4(slot + hs * 128 + ((c ^ (hs & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                        pk[4 * c + 3], rbar);
-          st_async_b32(slot + kSlotAlpha + 4 * hs, ex[0], rbar);
-          if (last) {
-            st_async_b32(slot + kSlotL0 + 4 * hs, ex[1], rbar);
-            st_async_b32(slot + kSlotL1 + 4 * hs, ex[2], rbar);
-            st_async_b32(slot + kSlotM + 4 * hs, ex[3], rbar);
+            for (int c = 0; c < 8; ++c)
+              st_async_v4(sl + h * 128 + ((c ^ (h & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                          pk[4 * c + 3], rbar);
+            st_async_b32(sl + kSlotAlpha + 4 * h, __float_as_uint(half == 0 ? alpha : 1.f), rbar);
           }
-          if (++pslot == kPSlots) { pslot = 0; pphase ^= 1; }
+          // the piece's row statistics travel with its last unit
+          if (last) {
+            const int u = unit + nunits - 1, slot = u % kPSlots;
+            if (!warp_wait(&ctrl->p_empty[slot], ((u / kPSlots) & 1) ^ 1, p.status, abort_flag)) goto score_done;
+            const uint32_t sl = peer_slots + slot * kSlotBytes;
+            const uint32_t rbar = mapa(smem_u32(&ctrl->p_full[slot]), 1);
+            st_async_b32(sl + (half ? kSlotL1 : kSlotL0) + 4 * h, __float_as_uint(lpart), rbar);
+            if (half == 0) st_async_b32(sl + kSlotM + 4 * h, __float_as_uint(m), rbar);
+          }
+          unit += nunits;
         }
       }
     }
@@ -509,30 +521,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // =========================== value CTA ===========================
     if (warp == 0) {
       if (lane == 0) {
-        int stage = 0;
+        // ring slot = latent chunks 0-3 or 4-7 of one 64-token block
+        int r = 0;
         uint32_t phase = 0;
         TileCursor ahead;
-        ahead.start(p.pieces, range.x, range.y, p.n_q);
-        int nb[kLookahead];
+        ahead.start(p.pieces, range.x, range.y, p.n_q, kBlk);
+        constexpr int kLA = 2 * kLookahead;   // blocks ahead
+        int raw[kLA];
+        uint32_t live = 0;
 #pragma unroll
-        for (int i = 0; i < kLookahead; ++i) {
-          nb[i] = block_of(ahead, p.table, p.max_blocks, p.num_blocks, p.status, false);
-          if (ahead.valid()) ahead.advance(p.pieces, p.n_q);
+        for (int u = 0; u < kLA; ++u) {
+          raw[u] = 0;
+          if (ahead.valid()) {
+            live |= 1u << u;
+            raw[u] = table_raw(p, ahead.b, ahead.t / kBlk);
+            ahead.advance(p.pieces, p.n_q);
+          }
         }
-        bool more = nb[0] >= 0;
-        while (more) {
+        while (live & 1u) {
 #pragma unroll
-          for (int u = 0; u < kLookahead; ++u) {
-            const int blk = nb[u];
-            if (blk < 0) { more = false; break; }
-            nb[u] = block_of(ahead, p.table, p.max_blocks, p.num_blocks, p.status, false);
-            if (ahead.valid()) ahead.advance(p.pieces, p.n_q);
-            if (!mbar_wait(&ctrl->v_empty[stage], phase ^ 1, p.status, abort_flag)) goto value_done;
-            mbar_arrive_expect_tx(&ctrl->v_full[stage], kVStageBytes);
-            tma_load_4d(smem + kOffStages + stage * kVStageBytes, &map4, &ctrl->v_full[stage], 0, 0, 0, blk);
-            tma_load_4d(smem + kOffStages + stage * kVStageBytes + 4 * kBoxBytes, &map4, &ctrl->v_full[stage], 0, 0, 4,
-                        blk);
-            if (++stage == kVStages) { stage = 0; phase ^= 1; }
+          for (int u = 0; u < kLA; ++u) {
+            if (!(live & (1u << u))) break;
+            const int blk = checked_block(p, raw[u], false);
+            live &= ~(1u << u);
+            if (ahead.valid()) {
+              live |= 1u << u;
+              raw[u] = table_raw(p, ahead.b, ahead.t / kBlk);
+              ahead.advance(p.pieces, p.n_q);
+            }
+#pragma unroll 1
+            for (int nh = 0; nh < 2; ++nh) {
+              if (!mbar_wait(&ctrl->v_empty[r], phase ^ 1, p.status, abort_flag)) goto value_done;
+              mbar_arrive_expect_tx(&ctrl->v_full[r], kSlotV);
+              tma_load_4d(smem + kOffV + r * kSlotV, &map4, &ctrl->v_full[r], 0, 0, 4 * nh, blk);
+              if (++r == kVRing) { r = 0; phase ^= 1; }
+            }
           }
         }
       }
@@ -540,8 +563,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // MMA warp: lane 0 issues, the whole warp waits and zeroes tail rows
       const uint32_t idesc = idesc_bf16(128, 256, false, true);
       const uint64_t pdesc0 = desc_sw128(smem_base + kOffSlots, 16, 1024);
-      const uint64_t vdesc0 = desc_sw128(smem_base + kOffStages, kBoxBytes, 1024);
-      int vstage = 0, pslot = 0;
+      const uint64_t vdesc0 = desc_sw128(smem_base + kOffV, kBoxBytes, 1024);
+      int r = 0, pslot = 0;
       uint32_t vphase = 0, pphase = 0, idle_phase = 0, done_phase = 0;
       for (int pi = range.x; pi < range.y; ++pi) {
         const Piece pc = p.pieces[pi];
@@ -549,22 +572,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
           const int valid = min(kBlk, pc.t_end - t);
           const bool first = (t == pc.t_begin), last = (t + kBlk >= pc.t_end);
-          if (!warp_wait(&ctrl->v_full[vstage], vphase, p.status, abort_flag)) goto value_mma_exit;
-          if (lane == 0) mbar_arrive_expect_tx(&ctrl->p_full[pslot], last ? kTxLast : kTxTile);
+          if (lane == 0) mbar_arrive_expect_tx(&ctrl->p_full[pslot], last ? kTxLast : kTxUnit);
           __syncwarp();
           if (!warp_wait(&ctrl->p_full[pslot], pphase, p.status, abort_flag)) goto value_mma_exit;
-          uint8_t* vst = smem + kOffStages + vstage * kVStageBytes;
           uint8_t* slot = smem + kOffSlots + pslot * kSlotBytes;
-          if (valid < kBlk) {
-            // tokens past the end of the sequence: zero their rows so 0 * garbage cannot reach O
-            const int nrow = kBlk - valid;
-            for (int e = lane; e < nrow * 64; e += 32) {
-              const int box = e / (nrow * 8), rem = e % (nrow * 8);
-              const int row = valid + rem / 8, ch = rem % 8;
-              *reinterpret_cast<uint4*>(vst + box * kBoxBytes + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-            }
-          }
-          // does any row's running max jump on this tile?
+          // does any row's running max jump on this unit?
           const float* alphas = reinterpret_cast<const float*>(slot + kSlotAlpha);
           const bool flag = __any_sync(0xffffffffu, alphas[lane] != 1.f || alphas[lane + 32] != 1.f ||
                                                         alphas[lane + 64] != 1.f || alphas[lane + 96] != 1.f);
@@ -577,10 +589,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ctrl->m_buf[i] = mm[i];
             }
           }
-          fence_proxy_async_smem();
           __syncwarp();
           if (flag && !first) {
-            // the running max jumped: O must be rescaled before this tile accumulates
+            // the running max jumped: O must be rescaled before this unit accumulates
             if (lane == 0) mma_commit(&ctrl->mma_idle);
             __syncwarp();
             if (!warp_wait(&ctrl->mma_idle, idle_phase, p.status, abort_flag)) goto value_mma_exit;
@@ -593,22 +604,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!warp_wait(&ctrl->done, done_phase, p.status, abort_flag)) goto value_mma_exit;
             done_phase ^= 1;
           }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint64_t pd = pdesc0 + (uint64_t)(pslot * (kSlotBytes >> 4));
-            const uint64_t vd = vdesc0 + (uint64_t)(vstage * (kVStageBytes >> 4));
+#pragma unroll 1
+          for (int nh = 0; nh < 2; ++nh) {
+            if (!warp_wait(&ctrl->v_full[r], vphase, p.status, abort_flag)) goto value_mma_exit;
+            if (valid < kBlk) {
+              // tokens past the end of the sequence: zero their rows so 0 * garbage cannot reach O
+              uint8_t* vst = smem + kOffV + r * kSlotV;
+              const int nrow = kBlk - valid;
+              for (int e = lane; e < nrow * 32; e += 32) {
+                const int box = e / (nrow * 8), rem = e % (nrow * 8);
+                const int row = valid + rem / 8, ch = rem % 8;
+                *reinterpret_cast<uint4*>(vst + box * kBoxBytes + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t pd = pdesc0 + (uint64_t)(pslot * (kSlotBytes >> 4));
+              const uint64_t vd = vdesc0 + (uint64_t)(r * (kSlotV >> 4));
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-#pragma unroll
-              for (int nh = 0; nh < 2; ++nh)
-                mma_ss(tmem + nh * 256, pd + (uint64_t)(s * 2),
-                       vd + (uint64_t)(nh * 4 * (kBoxBytes >> 4) + s * (2048 >> 4)), idesc,
+              for (int s = 0; s < 4; ++s)
+                mma_ss(tmem + nh * 256, pd + (uint64_t)(s * 2), vd + (uint64_t)(s * (2048 >> 4)), idesc,
                        (!first || s > 0) ? 1u : 0u);
-            mma_commit(&ctrl->v_empty[vstage]);
-            mma_commit_multicast(&ctrl->p_empty[pslot], 0x1);
+              mma_commit(&ctrl->v_empty[r]);
+            }
+            __syncwarp();
+            if (++r == kVRing) { r = 0; vphase ^= 1; }
           }
+          if (lane == 0) mma_commit_multicast(&ctrl->p_empty[pslot], 0x1);
           __syncwarp();
-          if (++vstage == kVStages) { vstage = 0; vphase ^= 1; }
           if (++pslot == kPSlots) { pslot = 0; pphase ^= 1; }
         }
         // piece finished: wait for the last accumulation, then hand O to the epilogue
@@ -679,7 +704,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (p.lse_out && half == 0) p.lse_out[(size_t)pc.item * kH + h] = lse;
           } else {
-            float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)pc.slot * kH + h) * kDC + half * 256);
+            // partial layout [slot][column / 4][row][4]: each store of a warp fills 512 contiguous bytes
+            float4* dst = reinterpret_cast<float4*>(p.part_o) + ((size_t)pc.slot * (kDC / 4) + half * 64) * kH + h;
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
               uint32_t r[32];
@@ -687,8 +713,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tmem_ld_wait();
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                dst[c * 8 + i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                             __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                dst[(size_t)(c * 8 + i) * kH] =
+                    make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
             }
             if (half == 0) p.part_lse[(size_t)pc.slot * kH + h] = lse;
           }
@@ -714,47 +741,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ split merge
-__global__ void __launch_bounds__(128) merge_kernel(const Piece* pieces, const int2* item_range, const float* part_o,
-                                                    const float* part_lse, bf16* o_lat, float* lse_out) {
-  const int item = blockIdx.x;
+// Block (item, g) merges columns [64 g, 64 g + 64) of all 128 heads; thread = head row.
+constexpr int kMergeGroups = kDC / 64;
+
+__global__ void __launch_bounds__(kH) merge_kernel(const Piece* pieces, const int2* item_range, const float* part_o,
+                                                   const float* part_lse, bf16* o_lat, float* lse_out) {
+  const int item = blockIdx.x, g = blockIdx.y, h = threadIdx.x;
   const int2 r = item_range[item];
   if (r.y == 1) return;  // written directly by the attention kernel
-  const int h = blockIdx.y * 4 + threadIdx.x / 32, lane = threadIdx.x & 31;
-  bf16* dst = o_lat + ((size_t)item * kH + h) * kDC;
+  uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)item * kH + h) * kDC + g * 64);
   if (r.y == 0) {
-    for (int i = lane; i < kDC; i += 32) dst[i] = __float2bfloat16_rn(0.f);
-    if (lse_out && lane == 0) lse_out[(size_t)item * kH + h] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+    if (lse_out && g == 0) lse_out[(size_t)item * kH + h] = -INFINITY;
     return;
   }
   float mx = -INFINITY;
   for (int k = 0; k < r.y; ++k) mx = fmaxf(mx, part_lse[(size_t)pieces[r.x + k].slot * kH + h]);
   float z = 0.f;
-  float acc[16];
+  float acc[64];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 64; ++i) acc[i] = 0.f;
   for (int k = 0; k < r.y; ++k) {
     const int slot = pieces[r.x + k].slot;
     const float w = expf(part_lse[(size_t)slot * kH + h] - mx);
     z += w;
-    const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)slot * kH + h) * kDC);
+    // partial layout [slot][column / 4][row][4]
+    const float4* src = reinterpret_cast<const float4*>(part_o) + ((size_t)slot * (kDC / 4) + g * 16) * kH + h;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 v = src[lane + 32 * i];
-      acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
-      acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
-      acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
-      acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
+    for (int j = 0; j < 16; ++j) {
+      const float4 v = src[(size_t)j * kH];
+      acc[4 * j] = fmaf(w, v.x, acc[4 * j]);
+      acc[4 * j + 1] = fmaf(w, v.y, acc[4 * j + 1]);
+      acc[4 * j + 2] = fmaf(w, v.z, acc[4 * j + 2]);
+      acc[4 * j + 3] = fmaf(w, v.w, acc[4 * j + 3]);
     }
   }
   const float inv = 1.f / z;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = 4 * (lane + 32 * i);
-    __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(dst + e);
-    d2[0] = __floats2bfloat162_rn(acc[4 * i] * inv, acc[4 * i + 1] * inv);
-    d2[1] = __floats2bfloat162_rn(acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+  for (int i = 0; i < 8; ++i) {
+    uint4 v;
+    v.x = pack_bf16x2(acc[8 * i] * inv, acc[8 * i + 1] * inv);
+    v.y = pack_bf16x2(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv);
+    v.z = pack_bf16x2(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv);
+    v.w = pack_bf16x2(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv);
+    dst[i] = v;
   }
-  if (lse_out && lane == 0) lse_out[(size_t)item * kH + h] = mx + logf(z);
+  if (lse_out && g == 0) lse_out[(size_t)item * kH + h] = mx + logf(z);
 }
 
 // ------------------------------------------------------------------ host side
@@ -854,15 +887,15 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   int2* cluster_range = reinterpret_cast<int2*>(ws + w.cluster_range);
   Piece* pieces = reinterpret_cast<Piece*>(ws + w.pieces);
 
-  // The pool viewed as [block][64-element chunk][token][element]; a box of 5 or 4 chunks lands
+  // The pool viewed as [block][64-element chunk][token][element]; a box of 1 or 4 chunks lands
   // as [chunk][token][128 B] with the 128-byte swizzle the MMA descriptors expect.
-  CUtensorMap map5, map4;
+  CUtensorMap map1, map4;
   const cuuint64_t dims[4] = {64, (cuuint64_t)kBlk, (cuuint64_t)kChunks, (cuuint64_t)cache.num_blocks};
   const cuuint64_t strides[3] = {(cuuint64_t)kRow * 2, 128, (cuuint64_t)kBlk * kRow * 2};
-  const cuuint32_t box5[4] = {64, (cuuint32_t)kBlk, (cuuint32_t)kKSplit, 1};
+  const cuuint32_t box1[4] = {64, (cuuint32_t)kBlk, 1, 1};
   const cuuint32_t box4[4] = {64, (cuuint32_t)kBlk, 4, 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
-  if (encode(&map5, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache.pool, dims, strides, box5, estride,
+  if (encode(&map1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache.pool, dims, strides, box1, estride,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
       encode(&map4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache.pool, dims, strides, box4, estride,
@@ -893,12 +926,12 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   prm.status = ctx.status;
   e = ensure_smem_limit((const void*)decode_tc_kernel, kSmemBytes, ctx.device);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, ctx.stream>>>(map5, map4, prm);
+  decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, ctx.stream>>>(map1, map4, prm);
   count_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  merge_kernel<<<dim3(items, kH / 4), 128, 0, ctx.stream>>>(pieces, item_range, prm.part_o, prm.part_lse,
+  merge_kernel<<<dim3(items, kMergeGroups), kH, 0, ctx.stream>>>(pieces, item_range, prm.part_o, prm.part_lse,
                                                             prm.o_lat, lse);
   count_launch();
   return cudaGetLastError();
