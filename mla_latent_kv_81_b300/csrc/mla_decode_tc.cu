@@ -41,7 +41,7 @@ constexpr int kThreads = 384;                       // warps 0-3: TMA, MMA, TMEM
 constexpr int kBoxBytes = 64 * 64 * 2;              // one swizzled [64 tokens x 64 elements] box
 constexpr int kChunks = kRow / 64;                  // 9 chunks per cached row: 8 latent + 1 positional
 constexpr int kSlotK = 2 * kBoxBytes;               // score ring slot: one chunk of a 128-token tile
-constexpr int kRing = 12;
+constexpr int kRing = 10;
 constexpr int kSlotV = 4 * kBoxBytes;               // value ring slot: four latent chunks of one block
 constexpr int kVRing = 5;
 constexpr int kPSlots = 3;                          // P units (64 tokens) in flight to the value CTA
@@ -52,10 +52,12 @@ constexpr int kOffQR = kCtrlBytes;                  // score CTA: positional par
 constexpr int kOffRing = kOffQR + kH * 128;
 constexpr int kOffV = kCtrlBytes;                   // value CTA
 constexpr int kOffSlots = kOffV + kVRing * kSlotV;
-constexpr int kSmemScore = kOffRing + kRing * kSlotK;
+constexpr int kOffStage = kOffRing + kRing * kSlotK;  // score CTA: each warpgroup's unit of P, laid out as a slot
+constexpr int kSmemScore = kOffStage + 2 * kSlotBytes;
 constexpr int kSmemValue = kOffSlots + kPSlots * kSlotBytes;
 constexpr int kSmemBytes = (kSmemScore > kSmemValue ? kSmemScore : kSmemValue) + 1024;  // + alignment slack
-static_assert(kOffRing % 1024 == 0 && kOffSlots % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle alignment");
+static_assert(kOffRing % 1024 == 0 && kOffSlots % 1024 == 0 && kOffStage % 1024 == 0 && kSlotBytes % 1024 == 0,
+              "swizzle alignment");
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTxUnit = 16384 + 512;
 constexpr uint32_t kTxLast = kTxUnit + 1536;
@@ -76,6 +78,7 @@ struct Ctrl {
   uint64_t k_full[kRing], k_empty[kRing];
   uint64_t s_full[2], s_empty[2];
   uint64_t q_ready;
+  uint64_t stage_free[2], stage_full[2];   // per warpgroup: its P staging buffer may be written / is written
   uint64_t xch[2];
   uint64_t p_empty[kPSlots];
   uint64_t v_full[kVRing], v_empty[kVRing];
@@ -292,6 +295,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctrl->xch[i], 256);
     }
     mbar_init(&ctrl->q_ready, 256);
+    for (int i = 0; i < 2; ++i) { mbar_init(&ctrl->stage_free[i], 1); mbar_init(&ctrl->stage_full[i], 128); }
     for (int i = 0; i < kPSlots; ++i) { mbar_init(&ctrl->p_empty[i], 1); mbar_init(&ctrl->p_full[i], 1); }
     for (int i = 0; i < kVRing; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
     mbar_init(&ctrl->mma_idle, 1);
@@ -385,21 +389,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int t = pc.t_begin; t < pc.t_end; t += kTile) {
             if (!mbar_wait(&ctrl->s_empty[sbuf], sphase ^ 1, p.status, abort_flag)) goto score_done;
             const uint32_t d = tmem + kSCol + sbuf * kTile;
+            // the tile's 9 chunks are accumulated in the order they land (their loads complete out of
+            // order), so a late chunk does not hold the slots of the chunks behind it
+            uint32_t pending = (1u << kChunks) - 1;
+            uint32_t acc = 0;
+            const long long t0 = clock64();
+            while (pending) {
+              bool progress = false;
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-              if (!mbar_wait(&ctrl->k_full[r], kphase, p.status, abort_flag)) goto score_done;
-              tc_fence_after();
-              const uint64_t kd = ring0 + (uint64_t)(r * (kSlotK >> 4));
+              for (int c = 0; c < kChunks; ++c) {
+                if (!(pending & (1u << c))) continue;
+                int rc = r + c;
+                uint32_t ph = kphase;
+                if (rc >= kRing) { rc -= kRing; ph ^= 1; }
+                if (!mbar_poll(smem_u32(&ctrl->k_full[rc]), ph)) continue;
+                tc_fence_after();
+                const uint64_t kd = ring0 + (uint64_t)(rc * (kSlotK >> 4));
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                if (c < kChunks - 1)
-                  mma_ts(d, tmem + kQCol + c * 32 + k * 8, kd + (uint64_t)(k * 2), idesc, (c | k) ? 1u : 0u);
-                else
-                  mma_ss(d, qr0 + (uint64_t)(k * 2), kd + (uint64_t)(k * 2), idesc, 1u);
+                for (int k = 0; k < 4; ++k) {
+                  if (c < kChunks - 1)
+                    mma_ts(d, tmem + kQCol + c * 32 + k * 8, kd + (uint64_t)(k * 2), idesc, (acc | k) ? 1u : 0u);
+                  else
+                    mma_ss(d, qr0 + (uint64_t)(k * 2), kd + (uint64_t)(k * 2), idesc, (acc | k) ? 1u : 0u);
+                }
+                acc = 1;
+                mma_commit(&ctrl->k_empty[rc]);
+                pending &= ~(1u << c);
+                progress = true;
               }
-              mma_commit(&ctrl->k_empty[r]);
-              if (++r == kRing) { r = 0; kphase ^= 1; }
+              if (!progress) {
+                // nothing landed: doze on the oldest outstanding chunk for a moment
+                int rc = r + __ffs(pending) - 1;
+                uint32_t ph = kphase;
+                if (rc >= kRing) { rc -= kRing; ph ^= 1; }
+                mbar_test_sleep(smem_u32(&ctrl->k_full[rc]), ph, 200u);
+                if (*abort_flag) goto score_done;
+                if (clock64() - t0 > kTimeoutCycles) {
+                  atomicOr(p.status, kFlagTimeout);
+                  *abort_flag = 1;
+                  goto score_done;
+                }
+              }
             }
+            r += kChunks;
+            if (r >= kRing) { r -= kRing; kphase ^= 1; }
             mma_commit(&ctrl->s_full[sbuf]);
             if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
           }
@@ -410,7 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
       const uint32_t peer_slots = mapa(smem_base + kOffSlots, 1);
       int sbuf = 0, tile = 0, unit = 0;
-      uint32_t sphase = 0;
+      uint32_t sphase = 0, stage_phase = 0;
       for (int pi = range.x; pi < range.y; ++pi) {
         const Piece pc = p.pieces[pi];
         if (pc.t_end <= pc.t_begin) continue;
@@ -491,30 +524,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pk[16 + i] = pack_bf16x2(p2, p3);
           }
           lpart += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-          // this half's unit of P (and its rescale factor) -> the value CTA's slot
+          // this half's unit of P (with its rescale factor and, on a piece's last tile, the row
+          // statistics) is written to the warpgroup's staging buffer in the value CTA's slot layout and
+          // shipped by one bulk copy: a few large DMA transfers instead of thousands of remote stores,
+          // which would hold up the MMA warp's tcgen05 instructions behind them
+          uint8_t* stage = smem + kOffStage + half * kSlotBytes;
+          const bool leader = (warp & 3) == 0 && lane == 0;
+          if (leader) {
+            bulk_wait_read_all();            // the previous tile's copies have read the buffer
+            mbar_arrive(&ctrl->stage_free[half]);
+          }
+          if (!warp_wait(&ctrl->stage_free[half], stage_phase, p.status, abort_flag)) goto score_done;
           if (half < nunits) {
-            const int u = unit + half, slot = u % kPSlots;
-            if (!warp_wait(&ctrl->p_empty[slot], ((u / kPSlots) & 1) ^ 1, p.status, abort_flag)) goto score_done;
-            const uint32_t sl = peer_slots + slot * kSlotBytes;
-            const uint32_t rbar = mapa(smem_u32(&ctrl->p_full[slot]), 1);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              st_async_v4(sl + h * 128 + ((c ^ (h & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                          pk[4 * c + 3], rbar);
-            st_async_b32(sl + kSlotAlpha + 4 * h, __float_as_uint(half == 0 ? alpha : 1.f), rbar);
+              *reinterpret_cast<uint4*>(stage + h * 128 + ((c ^ (h & 7)) << 4)) =
+                  make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            reinterpret_cast<float*>(stage + kSlotAlpha)[h] = half == 0 ? alpha : 1.f;
           }
-          // the piece's row statistics travel with its last unit
           if (last) {
-            const int u = unit + nunits - 1, slot = u % kPSlots;
-            if (!warp_wait(&ctrl->p_empty[slot], ((u / kPSlots) & 1) ^ 1, p.status, abort_flag)) goto score_done;
-            const uint32_t sl = peer_slots + slot * kSlotBytes;
-            const uint32_t rbar = mapa(smem_u32(&ctrl->p_full[slot]), 1);
-            st_async_b32(sl + (half ? kSlotL1 : kSlotL0) + 4 * h, __float_as_uint(lpart), rbar);
-            if (half == 0) st_async_b32(sl + kSlotM + 4 * h, __float_as_uint(m), rbar);
+            reinterpret_cast<float*>(stage + (half ? kSlotL1 : kSlotL0))[h] = lpart;
+            if (half == 0) reinterpret_cast<float*>(stage + kSlotM)[h] = m;
           }
+          fence_proxy_async_smem();
+          mbar_arrive(&ctrl->stage_full[half]);
+          if (leader) {
+            if (!mbar_wait(&ctrl->stage_full[half], stage_phase, p.status, abort_flag)) goto score_done;
+            if (half < nunits) {
+              const int u = unit + half, slot = u % kPSlots;
+              if (!mbar_wait(&ctrl->p_empty[slot], ((u / kPSlots) & 1) ^ 1, p.status, abort_flag)) goto score_done;
+              bulk_copy_to_peer(peer_slots + slot * kSlotBytes, stage, kSlotAlpha + kH * 4,
+                                mapa(smem_u32(&ctrl->p_full[slot]), 1));
+            }
+            if (last) {
+              const int u = unit + nunits - 1, slot = u % kPSlots;
+              if (!mbar_wait(&ctrl->p_empty[slot], ((u / kPSlots) & 1) ^ 1, p.status, abort_flag)) goto score_done;
+              const uint32_t rbar = mapa(smem_u32(&ctrl->p_full[slot]), 1);
+              const int lo = half ? kSlotL1 : kSlotL0;
+              bulk_copy_to_peer(peer_slots + slot * kSlotBytes + lo, stage + lo, kH * 4, rbar);
+              if (half == 0) bulk_copy_to_peer(peer_slots + slot * kSlotBytes + kSlotM, stage + kSlotM, kH * 4, rbar);
+            }
+            bulk_commit_group();
+          }
+          stage_phase ^= 1;
           unit += nunits;
         }
       }
+      // the staging buffers must outlive the copies reading them
+      if ((warp & 3) == 0 && lane == 0) bulk_wait_all();
     }
   score_done:;
   } else {
