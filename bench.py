@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
 DECODE_SOURCES = ["mla_latent_kv_81_b300/csrc/mla_decode_tc.cu", "mla_latent_kv_81_b300/csrc/mla_tc.cu",
-                  "mla_latent_kv_81_b300/csrc/mla_simt.cu"]
+                  "mla_latent_kv_81_b300/csrc/mla_simt.cu", "mla_latent_kv_81_b300/csrc/mla_sm100.cuh"]
 
 
 # ------------------------------------------------------------------ algorithmic work

@@ -163,6 +163,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __all_sync(0xffffffffu, ok);
 }
 
+// The same for barriers that only this CTA completes (cheaper CTA-scope acquire).
+__device__ __forceinline__ bool warp_wait_cta(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                              volatile int* abort_flag) {
+  const bool ok = mbar_wait_cta(bar, parity, status, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------ planner
 // One CTA of 1024 threads.  Cuts the visible 128-token tiles of all queries into C
 // equal contiguous ranges (cluster c gets global tiles [c*T/C, (c+1)*T/C))
@@ -362,7 +369,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
 #pragma unroll 1
             for (int c = 0; c < kChunks; ++c) {
-              if (!mbar_wait(&ctrl->k_empty[r], phase ^ 1, p.status, abort_flag)) goto score_done;
+              if (!mbar_wait_cta(&ctrl->k_empty[r], phase ^ 1, p.status, abort_flag)) goto score_done;
               uint8_t* dst = smem + kOffRing + r * kSlotK;
               mbar_arrive_expect_tx(&ctrl->k_full[r], b1 >= 0 ? 2 * kBoxBytes : kBoxBytes);
               tma_load_4d(dst, &map1, &ctrl->k_full[r], 0, 0, c, b0);
@@ -387,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&ctrl->q_ready, qphase, p.status, abort_flag)) goto score_done;
           qphase ^= 1;
           for (int t = pc.t_begin; t < pc.t_end; t += kTile) {
-            if (!mbar_wait(&ctrl->s_empty[sbuf], sphase ^ 1, p.status, abort_flag)) goto score_done;
+            if (!mbar_wait_cta(&ctrl->s_empty[sbuf], sphase ^ 1, p.status, abort_flag)) goto score_done;
             const uint32_t d = tmem + kSCol + sbuf * kTile;
             // the tile's 9 chunks are accumulated in the order they land (their loads complete out of
             // order), so a late chunk does not hold the slots of the chunks behind it
@@ -402,7 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int rc = r + c;
                 uint32_t ph = kphase;
                 if (rc >= kRing) { rc -= kRing; ph ^= 1; }
-                if (!mbar_poll(smem_u32(&ctrl->k_full[rc]), ph)) continue;
+                if (!mbar_poll_cta(smem_u32(&ctrl->k_full[rc]), ph)) continue;
                 tc_fence_after();
                 const uint64_t kd = ring0 + (uint64_t)(rc * (kSlotK >> 4));
 #pragma unroll
@@ -477,7 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int nunits = ntok > kBlk ? 2 : 1;
           const int valid = ntok - half * kBlk;   // valid columns of this half (may be <= 0)
           const bool first = (t == pc.t_begin), last = (t + kTile >= pc.t_end);
-          if (!warp_wait(&ctrl->s_full[sbuf], sphase, p.status, abort_flag)) goto score_done;
+          if (!warp_wait_cta(&ctrl->s_full[sbuf], sphase, p.status, abort_flag)) goto score_done;
           tc_fence_after();
           uint32_t sa[32], sb[32];   // columns 0-31 and 32-63 of this half
           tmem_ld32(lane_base + kSCol + sbuf * kTile + half * kBlk, sa);
@@ -503,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // exchange the half-row maxima with the partner thread of the other warpgroup
           ctrl->half_max[tile & 1][half][h] = hmax;
           mbar_arrive(&ctrl->xch[tile & 1]);
-          if (!warp_wait(&ctrl->xch[tile & 1], (tile >> 1) & 1, p.status, abort_flag)) goto score_done;
+          if (!warp_wait_cta(&ctrl->xch[tile & 1], (tile >> 1) & 1, p.status, abort_flag)) goto score_done;
           const float mx = fmaxf(ctrl->half_max[tile & 1][0][h], ctrl->half_max[tile & 1][1][h]);
           float alpha = 1.f;
           if (first) {
@@ -534,7 +541,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bulk_wait_read_all();            // the previous tile's copies have read the buffer
             mbar_arrive(&ctrl->stage_free[half]);
           }
-          if (!warp_wait(&ctrl->stage_free[half], stage_phase, p.status, abort_flag)) goto score_done;
+          if (!warp_wait_cta(&ctrl->stage_free[half], stage_phase, p.status, abort_flag)) goto score_done;
           if (half < nunits) {
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -549,7 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           mbar_arrive(&ctrl->stage_full[half]);
           if (leader) {
-            if (!mbar_wait(&ctrl->stage_full[half], stage_phase, p.status, abort_flag)) goto score_done;
+            if (!mbar_wait_cta(&ctrl->stage_full[half], stage_phase, p.status, abort_flag)) goto score_done;
             if (half < nunits) {
               const int u = unit + half, slot = u % kPSlots;
               if (!mbar_wait(&ctrl->p_empty[slot], ((u / kPSlots) & 1) ^ 1, p.status, abort_flag)) goto score_done;
@@ -608,7 +615,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
 #pragma unroll 1
             for (int nh = 0; nh < 2; ++nh) {
-              if (!mbar_wait(&ctrl->v_empty[r], phase ^ 1, p.status, abort_flag)) goto value_done;
+              if (!mbar_wait_cta(&ctrl->v_empty[r], phase ^ 1, p.status, abort_flag)) goto value_done;
               mbar_arrive_expect_tx(&ctrl->v_full[r], kSlotV);
               tma_load_4d(smem + kOffV + r * kSlotV, &map4, &ctrl->v_full[r], 0, 0, 4 * nh, blk);
               if (++r == kVRing) { r = 0; phase ^= 1; }
@@ -651,19 +658,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // the running max jumped: O must be rescaled before this unit accumulates
             if (lane == 0) mma_commit(&ctrl->mma_idle);
             __syncwarp();
-            if (!warp_wait(&ctrl->mma_idle, idle_phase, p.status, abort_flag)) goto value_mma_exit;
+            if (!warp_wait_cta(&ctrl->mma_idle, idle_phase, p.status, abort_flag)) goto value_mma_exit;
             idle_phase ^= 1;
             if (lane == 0) {
               ctrl->cmd = kCmdRescale;
               ctrl->cmd_slot = pslot;
               mbar_arrive(&ctrl->work);
             }
-            if (!warp_wait(&ctrl->done, done_phase, p.status, abort_flag)) goto value_mma_exit;
+            if (!warp_wait_cta(&ctrl->done, done_phase, p.status, abort_flag)) goto value_mma_exit;
             done_phase ^= 1;
           }
 #pragma unroll 1
           for (int nh = 0; nh < 2; ++nh) {
-            if (!warp_wait(&ctrl->v_full[r], vphase, p.status, abort_flag)) goto value_mma_exit;
+            if (!warp_wait_cta(&ctrl->v_full[r], vphase, p.status, abort_flag)) goto value_mma_exit;
             if (valid < kBlk) {
               // tokens past the end of the sequence: zero their rows so 0 * garbage cannot reach O
               uint8_t* vst = smem + kOffV + r * kSlotV;
@@ -696,14 +703,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // piece finished: wait for the last accumulation, then hand O to the epilogue
         if (lane == 0) mma_commit(&ctrl->mma_idle);
         __syncwarp();
-        if (!warp_wait(&ctrl->mma_idle, idle_phase, p.status, abort_flag)) goto value_mma_exit;
+        if (!warp_wait_cta(&ctrl->mma_idle, idle_phase, p.status, abort_flag)) goto value_mma_exit;
         idle_phase ^= 1;
         if (lane == 0) {
           ctrl->cmd = kCmdEpilogue;
           ctrl->cmd_piece = pi;
           mbar_arrive(&ctrl->work);
         }
-        if (!warp_wait(&ctrl->done, done_phase, p.status, abort_flag)) goto value_mma_exit;
+        if (!warp_wait_cta(&ctrl->done, done_phase, p.status, abort_flag)) goto value_mma_exit;
         done_phase ^= 1;
       }
     value_mma_exit:
@@ -716,7 +723,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16) + half * 256;
       uint32_t wphase = 0;
       while (true) {
-        if (!warp_wait(&ctrl->work, wphase, p.status, abort_flag)) break;
+        if (!warp_wait_cta(&ctrl->work, wphase, p.status, abort_flag)) break;
         wphase ^= 1;
         const int cmd = *reinterpret_cast<volatile int*>(&ctrl->cmd);
         if (cmd == kCmdExit) break;
