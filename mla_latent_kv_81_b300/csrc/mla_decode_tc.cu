@@ -493,10 +493,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(&ctrl->s_empty[sbuf]);
           if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
+          if (valid < kBlk) {
+            // columns past the end of the piece (only in its last tile)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            sa[i] = __float_as_uint(i < valid ? __uint_as_float(sa[i]) * p.scale_log2 : -INFINITY);
-            sb[i] = __float_as_uint(i + 32 < valid ? __uint_as_float(sb[i]) * p.scale_log2 : -INFINITY);
+            for (int i = 0; i < 32; ++i) {
+              if (i >= valid) sa[i] = __float_as_uint(-INFINITY);
+              if (i + 32 >= valid) sb[i] = __float_as_uint(-INFINITY);
+            }
           }
           float mx8[8];
 #pragma unroll
@@ -511,7 +514,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ctrl->half_max[tile & 1][half][h] = hmax;
           mbar_arrive(&ctrl->xch[tile & 1]);
           if (!warp_wait_cta(&ctrl->xch[tile & 1], (tile >> 1) & 1, p.status, abort_flag)) goto score_done;
-          const float mx = fmaxf(ctrl->half_max[tile & 1][0][h], ctrl->half_max[tile & 1][1][h]);
+          // raw scores: the positive scale commutes with the maximum
+          const float mx = fmaxf(ctrl->half_max[tile & 1][0][h], ctrl->half_max[tile & 1][1][h]) * p.scale_log2;
           float alpha = 1.f;
           if (first) {
             m = mx;
@@ -522,10 +526,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           uint32_t pk[32];
           float ps[4] = {0.f, 0.f, 0.f, 0.f};
+          const float sc = p.scale_log2;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(__uint_as_float(sa[2 * i]) - m), p1 = ex2(__uint_as_float(sa[2 * i + 1]) - m);
-            const float p2 = ex2(__uint_as_float(sb[2 * i]) - m), p3 = ex2(__uint_as_float(sb[2 * i + 1]) - m);
+            const float p0 = ex2(fmaf(__uint_as_float(sa[2 * i]), sc, -m));
+            const float p1 = ex2(fmaf(__uint_as_float(sa[2 * i + 1]), sc, -m));
+            const float p2 = ex2(fmaf(__uint_as_float(sb[2 * i]), sc, -m));
+            const float p3 = ex2(fmaf(__uint_as_float(sb[2 * i + 1]), sc, -m));
             ps[i & 3] += (p0 + p1) + (p2 + p3);
             pk[i] = pack_bf16x2(p0, p1);
             pk[16 + i] = pack_bf16x2(p2, p3);
@@ -805,35 +812,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ split merge
-// Block (item, g) merges columns [64 g, 64 g + 64) of all 128 heads; thread = head row.
-constexpr int kMergeGroups = kDC / 64;
+// Block (item, g) merges columns [16 g, 16 g + 16) of all 128 heads; thread = head row.
+constexpr int kMergeGroups = kDC / 16;
 
 __global__ void __launch_bounds__(kH) merge_kernel(const Piece* pieces, const int2* item_range, const float* part_o,
                                                    const float* part_lse, bf16* o_lat, float* lse_out) {
   const int item = blockIdx.x, g = blockIdx.y, h = threadIdx.x;
   const int2 r = item_range[item];
   if (r.y == 1) return;  // written directly by the attention kernel
-  uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)item * kH + h) * kDC + g * 64);
+  uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)item * kH + h) * kDC + g * 16);
   if (r.y == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 2; ++i) dst[i] = make_uint4(0, 0, 0, 0);
     if (lse_out && g == 0) lse_out[(size_t)item * kH + h] = -INFINITY;
     return;
   }
   float mx = -INFINITY;
   for (int k = 0; k < r.y; ++k) mx = fmaxf(mx, part_lse[(size_t)pieces[r.x + k].slot * kH + h]);
   float z = 0.f;
-  float acc[64];
+  float acc[16];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
   for (int k = 0; k < r.y; ++k) {
     const int slot = pieces[r.x + k].slot;
     const float w = expf(part_lse[(size_t)slot * kH + h] - mx);
     z += w;
     // partial layout [slot][column / 4][row][4]
-    const float4* src = reinterpret_cast<const float4*>(part_o) + ((size_t)slot * (kDC / 4) + g * 16) * kH + h;
+    const float4* src = reinterpret_cast<const float4*>(part_o) + ((size_t)slot * (kDC / 4) + g * 4) * kH + h;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 4; ++j) {
       const float4 v = src[(size_t)j * kH];
       acc[4 * j] = fmaf(w, v.x, acc[4 * j]);
       acc[4 * j + 1] = fmaf(w, v.y, acc[4 * j + 1]);
@@ -843,7 +850,7 @@ __global__ void __launch_bounds__(kH) merge_kernel(const Piece* pieces, const in
   }
   const float inv = 1.f / z;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 2; ++i) {
     uint4 v;
     v.x = pack_bf16x2(acc[8 * i] * inv, acc[8 * i + 1] * inv);
     v.y = pack_bf16x2(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv);
