@@ -108,6 +108,13 @@ struct Params {
   uint32_t* status;
 };
 
+// Maximum of three floats in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Walks a cluster's pieces in steps of `step` tokens.
@@ -503,13 +510,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           float mx8[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            mx8[i] = fmaxf(fmaxf(fmaxf(__uint_as_float(sa[i]), __uint_as_float(sa[i + 8])),
-                                 fmaxf(__uint_as_float(sa[i + 16]), __uint_as_float(sa[i + 24]))),
-                           fmaxf(fmaxf(__uint_as_float(sb[i]), __uint_as_float(sb[i + 8])),
-                                 fmaxf(__uint_as_float(sb[i + 16]), __uint_as_float(sb[i + 24]))));
-          const float hmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int i = 0; i < 8; ++i) {
+            const float t1 = max3f(__uint_as_float(sa[i]), __uint_as_float(sa[i + 8]), __uint_as_float(sa[i + 16]));
+            const float t2 = max3f(__uint_as_float(sb[i]), __uint_as_float(sb[i + 8]), __uint_as_float(sb[i + 16]));
+            mx8[i] = max3f(max3f(t1, t2, __uint_as_float(sa[i + 24])), __uint_as_float(sb[i + 24]), t1);
+          }
+          const float hmax = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
           // exchange the half-row maxima with the partner thread of the other warpgroup
           ctrl->half_max[tile & 1][half][h] = hmax;
           mbar_arrive(&ctrl->xch[tile & 1]);
@@ -525,19 +531,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             m = mx;
           }
           uint32_t pk[32];
-          float ps[4] = {0.f, 0.f, 0.f, 0.f};
-          const float sc = p.scale_log2;
+          // paired fp32 arithmetic: one instruction per two columns for the scaling and the row sum
+          const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
+          float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(sa[2 * i]), sc, -m));
-            const float p1 = ex2(fmaf(__uint_as_float(sa[2 * i + 1]), sc, -m));
-            const float p2 = ex2(fmaf(__uint_as_float(sb[2 * i]), sc, -m));
-            const float p3 = ex2(fmaf(__uint_as_float(sb[2 * i + 1]), sc, -m));
-            ps[i & 3] += (p0 + p1) + (p2 + p3);
-            pk[i] = pack_bf16x2(p0, p1);
-            pk[16 + i] = pack_bf16x2(p2, p3);
+            const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sa[2 * i]), __uint_as_float(sa[2 * i + 1])), sc2, nm2);
+            const float2 xb = __ffma2_rn(make_float2(__uint_as_float(sb[2 * i]), __uint_as_float(sb[2 * i + 1])), sc2, nm2);
+            const float2 pa = make_float2(ex2(xa.x), ex2(xa.y)), pb = make_float2(ex2(xb.x), ex2(xb.y));
+            ps2[i & 1] = __fadd2_rn(ps2[i & 1], __fadd2_rn(pa, pb));
+            pk[i] = pack_bf16x2(pa.x, pa.y);
+            pk[16 + i] = pack_bf16x2(pb.x, pb.y);
           }
-          lpart += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          lpart += (ps2[0].x + ps2[0].y) + (ps2[1].x + ps2[1].y);
           // this half's unit of P (with its rescale factor and, on a piece's last tile, the row
           // statistics) is written to the warpgroup's staging buffer in the value CTA's slot layout and
           // shipped by one bulk copy: a few large DMA transfers instead of thousands of remote stores,
