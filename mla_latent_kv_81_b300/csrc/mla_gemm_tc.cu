@@ -364,6 +364,8 @@ struct GemmPlan {
 
 // Tile and split a problem so that the SMs are covered about four units deep
 // (direct = no k-split: the GEMM stores bf16 itself).
+constexpr int kMinKbPerSplit = 8;   // 512 of K: 128 KB of a 128-row bf16 weight tile per split
+
 GemmPlan plan_gemm(int M, int N, int K, int G, bool a_mn, bool direct, int sm_count) {
   GemmPlan p{};
   GemmArgs& a = p.args;
@@ -376,11 +378,14 @@ GemmPlan plan_gemm(int M, int N, int K, int G, bool a_mn, bool direct, int sm_co
   a.m_tiles1 = a.m_tiles;
   a.kb = K / 64;
   const long long base = (long long)G * a.m_tiles * a.n_tiles;
-  // the fewest k-splits whose units fill the waves of SMs at least 90%
+  // the fewest k-splits whose units fill the waves of SMs at least 90%, but no split shallower than
+  // kMinKbPerSplit k-blocks: a thinner split costs more in fp32 partials and their reduction than its
+  // extra parallelism saves on a small weight
   int splits = 1;
   if (!direct) {
     double best = 0.0;
-    for (int s = 1; s <= a.kb && s <= 64; ++s) {
+    const int max_splits = a.kb / kMinKbPerSplit > 1 ? a.kb / kMinKbPerSplit : 1;
+    for (int s = 1; s <= max_splits && s <= 64; ++s) {
       const long long u = base * s;
       const double eff = (double)u / ((double)sm_count * ((u + sm_count - 1) / sm_count));
       if (eff > best + 1e-9) { best = eff; splits = s; }
