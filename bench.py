@@ -187,6 +187,22 @@ def oracle_sample(p: I.Problem, budget_s: float, heads_per_step: int | None = No
     return done_tok / elapsed, desc, threads, times
 
 
+# ------------------------------------------------------------------ multi-rank arithmetic
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest rank sets the job time)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_rate(tokens_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Cached tokens attended per second by all ranks together (replicas: every rank does the same work)."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 # ------------------------------------------------------------------ main paths
 def run_reference(args, rank: int, world: int):
     if rank != 0:
@@ -298,15 +314,10 @@ def run_ours(args, rank: int, world: int):
     launches = launches_per_step * args.steps
     ms_total = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
-    if dist is not None:
-        t = torch.tensor([ms_total, statistics.mean(dec_ms)], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total, dec_mean = float(t[0]), float(t[1])
-    else:
-        dec_mean = statistics.mean(dec_ms)
+    ms_total, dec_mean = max_over_ranks([ms_total, statistics.mean(dec_ms)], dist, "cuda")
     ms_step = ms_total / args.steps
     tokens = alg["cached_tokens"] * world
-    value = tokens / (ms_step * 1e-3)
+    value = whole_job_rate(alg["cached_tokens"], world, ms_step)
 
     # ---- end to end through the public API from pinned host buffers
     x_host = L.x_q.cpu().pin_memory()
@@ -324,11 +335,7 @@ def run_ours(args, rank: int, world: int):
         out_host.copy_(L.out, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], dist, "cuda")[0]
     code, flags = M.mla_get_device_status()
     if code != 0:
         raise RuntimeError(f"device status after timing: {M.mla_status_string(code)} ({flags})")
