@@ -143,6 +143,28 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample_absorbed(p: I.Problem, budget_s: float):
+    """Time the float64 oracle's absorbed form (query folded through W_UK, attention in latent space,
+    all heads of one sequence per step) until `budget_s`.  Returns (cached tokens per second, steps)."""
+    from oracle import mla_oracle as O
+    d, W = p.dims, p.weights
+    n_q, H = p.w.n_q, d.n_heads
+    scale = O.softmax_scale(d.qk_nope, d.d_rope)
+    done_tok, elapsed, steps, b = 0.0, 0.0, 0, 0
+    while elapsed < budget_s:
+        rows = I.draw_latent_rows(p.w, b, int(p.kv_len[b])).astype(np.float64)
+        sl = slice(b * n_q, (b + 1) * n_q)
+        t0 = time.perf_counter()
+        q_nope, q_rope = O.project_query(p.x_q[sl], W["W_Q"], W["W_QR"], p.q_pos[sl], H, d.rope_base)
+        q_abs = O.absorb_query(q_nope, W["W_UK"])
+        O.attend_latent(q_abs, q_rope, rows[:, :d.d_c], rows[:, d.d_c:], int(p.kv_len[b]), scale)
+        elapsed += time.perf_counter() - t0
+        done_tok += float(p.kv_len[b])
+        steps += 1
+        b = (b + 1) % p.w.batch
+    return done_tok / elapsed, steps
+
+
 def oracle_sample(p: I.Problem, budget_s: float, heads_per_step: int | None = None, max_steps: int | None = None):
     """Time the float64 oracle (explicit form, as it stands) on whole heads of whole
     sequences of the workload until `budget_s` or `max_steps` is reached.
@@ -373,11 +395,77 @@ def run_ours(args, rank: int, world: int):
     }
     if not args.no_cpu_baseline:
         rate, desc, threads, _ = oracle_sample(p, args.cpu_budget, heads_per_step=8)
+        abs_rate, abs_steps = oracle_sample_absorbed(p, max(1.0, args.cpu_budget / 3))
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-                                "sample": desc + f"; BLAS threads {threads}"}
+                                "sample": desc + f"; BLAS threads {threads}",
+                                "absorbed": {"value": abs_rate, "unit": UNIT,
+                                             "sample": f"absorbed-form oracle (float64, all heads) over {abs_steps} "
+                                                       f"whole sequence(s)"}}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_sweep(args):
+    """One JSON line per workload: the decode call (planner + attention + merge) as the median of
+    `--sweep-reps` runs with L2 flushed before each (a 256 MB write outside the timed region), its
+    cached tokens/s, algorithmic GB/s and roofline fraction, and the projection calls timed the same way."""
+    import torch
+    import mla_harness as Hn
+    import mla_latent_kv_81_b300 as M
+
+    hbm_peak, tf_peak, peak_kind = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    for name, w in I.WORKLOADS.items():
+        p = I.make_problem(w)
+        L = Hn.DeviceLayer(p)
+        L.fill()
+        L.step(with_lse=False)
+        n = L.x_q.shape[0]
+        alg = decode_algorithmic(p)
+        t_dec = timed(lambda: L.attend(with_lse=False), args.sweep_reps)
+        proj = {}
+        if p.w.n_append:
+            wsc = L._ws("c", M.mla_compress_workspace_bytes(L.cfg, n))
+            proj["compress_append"] = timed(lambda: M.mla_compress_append(
+                L.cfg, L.x_q, L.W["W_DKV"], L.W["W_KR"], L.app_seq, L.app_pos, L.rope, L.cache, ws=wsc), args.sweep_reps)
+        wsa = L._ws("a", M.mla_absorb_workspace_bytes(L.cfg, n))
+        proj["absorb_query"] = timed(lambda: M.mla_absorb_query(
+            L.cfg, L.x_q, L.W["W_Q"], L.W["W_QR"], L.W["W_UK"], L.q_pos, L.rope, L.q, ws=wsa), args.sweep_reps)
+        wso = L._ws("o", M.mla_output_workspace_bytes(L.cfg, n))
+        proj["output_project"] = timed(lambda: M.mla_output_project(
+            L.cfg, L.o_lat, L.W["W_UV"], L.W["W_O"], L.out, ws=wso), args.sweep_reps)
+        code, flags = M.mla_get_device_status()
+        if code != 0:
+            raise RuntimeError(f"{name}: device status {M.mla_status_string(code)} ({flags})")
+        t_roof = max(alg["bytes"] / (hbm_peak * 1e9), alg["flops"] / (tf_peak * 1e12))
+        bound = "hbm" if alg["bytes"] / (hbm_peak * 1e9) >= alg["flops"] / (tf_peak * 1e12) else "tensor"
+        print(json.dumps({
+            "sweep": name, "dtype": w.dtype, "config": workload_config(w, p), "decode_ms": t_dec,
+            "cached_tokens_per_s": alg["cached_tokens"] / (t_dec * 1e-3),
+            "achieved_gbs": alg["bytes"] / (t_dec * 1e-3) / 1e9,
+            "achieved_tflops": alg["flops"] / (t_dec * 1e-3) / 1e12,
+            "roofline": {"bound": bound, "t_roof_ms": t_roof * 1e3, "frac": t_roof / (t_dec * 1e-3),
+                         "peaks": f"{peak_kind}: {hbm_peak} GB/s, {tf_peak} TFLOP/s bf16"},
+            "projections_ms": proj, "timing": f"median of {args.sweep_reps}, L2 flushed (256 MB write) before each"}),
+            flush=True)
+        del L
+        torch.cuda.empty_cache()
 
 
 def main():
@@ -389,12 +477,18 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of CPU oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the step benchmark, one JSON line per workload (decode call and projections)")
+    ap.add_argument("--sweep-reps", type=int, default=50)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    if args.impl == "reference":
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world)
