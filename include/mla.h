@@ -162,7 +162,12 @@ size_t mla_decode_workspace_bytes(const mla_config* cfg, int batch, int n_q, int
  *   lse     optional device fp32 [batch][n_q][n_heads] (natural log of the
  *           softmax normaliser of the scaled scores; -inf when nothing is
  *           visible), or NULL
- * A query with no visible token gets o_lat = 0. */
+ * A query with no visible token gets o_lat = 0.
+ * Reproducibility: on the tensor-core path each 128-token score tile sums its
+ * nine 64-element chunks in the order their loads complete, so two calls on
+ * the same inputs may differ in the last bits of the fp32 scores (and, through
+ * bf16 rounding of P and o_lat, by up to about one bf16 ulp); the result is
+ * otherwise independent of how the sequences are split across CTAs. */
 mla_status mla_decode_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache,
                                 const int32_t* kv_len, int batch, int n_q, void* o_lat, float* lse,
                                 void* workspace, size_t workspace_bytes, mla_stream_t stream);
