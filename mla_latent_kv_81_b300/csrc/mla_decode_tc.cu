@@ -14,9 +14,9 @@
 //     128-token tiles (two blocks) through a ring of 16 KB chunk slots with
 //     TMA, computes S = Q K^T with N = 128 MMAs (the tensor core runs N = 64
 //     at about 60% of its rate), and runs the online softmax with two threads
-//     per head row (one per 64-token half); each half is one unit of bf16 P
-//     that the softmax threads push, with the per-row rescale factor, into the
-//     value CTA's shared memory with st.async;
+//     per head row (one per 64-token half); each half is one unit of bf16 P,
+//     staged with its per-row rescale factor in shared memory and shipped to
+//     the value CTA's shared memory by one bulk copy;
 //   * the value CTA (rank 1) streams the [64 x 512] latent part of every block
 //     as two 32 KB halves and accumulates O += P V in all 512 TMEM columns;
 //     two warpgroups rescale O when the running maximum jumps (rarely) and
