@@ -36,8 +36,7 @@ DEFAULT_WORKLOAD = "dsv2_b64_ctx8192"
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
-DECODE_SOURCES = ["mla_latent_kv_81_b300/csrc/mla_decode_tc.cu", "mla_latent_kv_81_b300/csrc/mla_tc.cu",
-                  "mla_latent_kv_81_b300/csrc/mla_simt.cu", "mla_latent_kv_81_b300/csrc/mla_sm100.cuh"]
+DECODE_SOURCES = ["mla_latent_kv_81_b300/csrc/mla_decode_tc.cu", "mla_latent_kv_81_b300/csrc/mla_sm100.cuh"]
 
 
 # ------------------------------------------------------------------ algorithmic work
@@ -239,12 +238,16 @@ def run_reference(args, rank: int, world: int):
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, p),
+        "config": dict(workload_config(w, p), parallelism=parallelism(world)),
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc + f"; BLAS threads {threads}"},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def parallelism(world: int) -> str:
+    return f"replicas x{world}" if world > 1 else "single GPU"
 
 
 def workload_config(w: I.Workload, p: I.Problem) -> dict:
@@ -285,7 +288,7 @@ def run_ours(args, rank: int, world: int):
 
     for _ in range(args.warmup):
         L.step(with_lse=False)
-    code, flags = M.mla_get_device_status()
+    code, flags = L.status()
     if code != 0:
         raise RuntimeError(f"device status after warm-up: {M.mla_status_string(code)} ({flags})")
 
@@ -358,7 +361,7 @@ def run_ours(args, rank: int, world: int):
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], dist, "cuda")[0]
-    code, flags = M.mla_get_device_status()
+    code, flags = L.status()
     if code != 0:
         raise RuntimeError(f"device status after timing: {M.mla_status_string(code)} ({flags})")
 
@@ -387,7 +390,7 @@ def run_ours(args, rank: int, world: int):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": p.w.dtype, "data": "synthetic (seeded Gaussian activations, weights, latents)",
-        "config": dict(workload_config(w, p), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "config": dict(workload_config(w, p), parallelism=parallelism(world)),
         "roofline": roof, "clocks": clk,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -450,7 +453,7 @@ def run_sweep(args):
         wso = L._ws("o", M.mla_output_workspace_bytes(L.cfg, n))
         proj["output_project"] = timed(lambda: M.mla_output_project(
             L.cfg, L.o_lat, L.W["W_UV"], L.W["W_O"], L.out, ws=wso), args.sweep_reps)
-        code, flags = M.mla_get_device_status()
+        code, flags = L.status()
         if code != 0:
             raise RuntimeError(f"{name}: device status {M.mla_status_string(code)} ({flags})")
         t_roof = max(alg["bytes"] / (hbm_peak * 1e9), alg["flops"] / (tf_peak * 1e12))

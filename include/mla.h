@@ -20,22 +20,35 @@
  * Conventions shared by every call
  *   - All pointers named d_* or documented as "device" are device pointers on
  *     the current CUDA device; the caller allocates and owns them.  The
- *     library never allocates device memory; calls that need scratch take a
+ *     library never allocates device memory; every compute call takes a
  *     caller-owned workspace whose size the matching *_workspace_bytes()
- *     returns.
+ *     returns (0 means the configuration is invalid or unsupported).
+ *   - Every workspace begins with a 256-byte header whose first 32-bit word is
+ *     the device status word of the calls made with that workspace.  A new
+ *     workspace must start with that word at zero (e.g. cudaMemsetAsync of its
+ *     first 4 bytes); calls only OR flags into it and mla_get_device_status()
+ *     clears it.  Calls that share a workspace share its word; calls with
+ *     different workspaces (on different streams, say) never see each
+ *     other's flags.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  Argument errors are detected on the host and
  *     returned before anything is launched.
  *   - Storage dtype (mla_config.dtype) applies to activations, weights, the
  *     cache, queries and outputs alike; accumulation is always fp32.  bf16
  *     results are rounded to nearest even.
+ *   - bf16 runs on the sm_103a tensor-core kernels, which cover the
+ *     DeepSeek-V2 head shapes (128 heads, d_c = 512, d_rope = 64, 64-token
+ *     blocks, projection widths that are multiples of 64); any other bf16
+ *     shape returns MLA_ERR_UNSUPPORTED.  fp32 runs on CUDA-core kernels at
+ *     any shape (tensor cores cannot hold fp32 operands at fp32 accuracy).
  *   - Weights are stored row-major as [out_features][in_features]; the
  *     per-head up-projections as [n_heads][out][d_c].
  *   - Device pointers must be 16-byte aligned.
  *   - Device-side index problems (a block-table entry outside the pool, a
  *     position outside a sequence's blocks, a sequence index outside the
  *     batch) never fault: the offending access is skipped and a flag is set
- *     that mla_get_device_status() reports.
+ *     in the call's status word.  Every wait inside a kernel is bounded (about
+ *     2 s); one that runs out sets a timeout flag and the kernel returns.
  */
 #ifndef MLA_H_
 #define MLA_H_
@@ -53,7 +66,7 @@ typedef struct CUstream_st* mla_stream_t;
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, inconsistent config        */
-  MLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. odd d_rope)                  */
+  MLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (odd d_rope, bf16 outside the tensor-core shapes) */
   MLA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed                         */
   MLA_ERR_TIMEOUT = 4,       /* device: a bounded wait gave up (reported by get_device_status) */
   MLA_ERR_DEVICE_INDEX = 5,  /* device: an out-of-range index was skipped                    */
@@ -185,10 +198,25 @@ mla_status mla_output_project(const mla_config* cfg, const void* o_lat, const vo
                               void* out, int N, void* workspace, size_t workspace_bytes,
                               mla_stream_t stream);
 
-/* Synchronise `stream`, then read and clear the current device's error word.
- * Returns MLA_OK, MLA_ERR_DEVICE_INDEX or MLA_ERR_TIMEOUT (the first set);
- * *flags (if not NULL) receives the raw bit set (bit 0 index, bit 1 timeout). */
-mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags);
+/* Synchronise `stream`, then read and clear the status word of `workspace`
+ * (the word in its header), or, when workspace is NULL, the library's own word
+ * on the current device, which only mla_compress_append_noalloc writes.
+ * Returns MLA_OK, MLA_ERR_DEVICE_INDEX or MLA_ERR_TIMEOUT (index takes
+ * precedence); *flags (if not NULL) receives the raw bit set (bit 0 index,
+ * bit 1 timeout).  Order the read after the calls it should cover: pass the
+ * stream they ran on. */
+mla_status mla_get_device_status(const void* workspace, mla_stream_t stream, uint32_t* flags);
+
+/* Self-check of the failure detection (no counterpart on the pages): launch one
+ * thread that waits on an mbarrier nothing ever completes, using the same
+ * bounded-wait routine as every kernel of the library but with a limit of
+ * `limit_cycles` SM cycles (10^4 .. 2*10^8, i.e. at most ~0.1 s) instead of
+ * ~2 s.  The wait gives up, sets the timeout flag in the workspace's status
+ * word and the kernel returns, leaving the context usable;
+ * mla_get_device_status(workspace, ...) then reports MLA_ERR_TIMEOUT.
+ * workspace: at least the 256-byte header, its status word zero. */
+mla_status mla_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_cycles,
+                                     mla_stream_t stream);
 
 /* mla_compress_append without a workspace argument.  No counterpart on the pages:
  * an interface for callers that cannot allocate device memory, for example code
@@ -196,12 +224,16 @@ mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags);
  * set up at start-up (inference servers, embedded runtimes, other languages'
  * runtimes holding only raw device pointers), or that may not call cudaMalloc
  * on the decode path because it would synchronise the device.
- * Same operation, arguments and error behaviour as mla_compress_append, except:
+ * Same operation and arguments as mla_compress_append, and the same argument
+ * checks in the same order, except:
  *   - the fp32 scratch lives in one fixed 16 MiB array inside the library
  *     (every GPU that loads the library holds it until the process exits);
  *     a call whose scratch would exceed it (mla_compress_workspace_bytes(cfg, T)
- *     > 16 MiB) returns MLA_ERR_WORKSPACE without touching the GPU; with the
- *     DeepSeek-V2 shape every call of up to 1024 tokens fits;
+ *     minus the 256-byte header > 16 MiB) returns MLA_ERR_WORKSPACE without
+ *     touching the GPU; with the DeepSeek-V2 shape on a 148-SM B300 every call
+ *     of up to 1024 tokens fits;
+ *   - device-side flags go to the library's own status word, read with
+ *     mla_get_device_status(NULL, stream, ...);
  *   - the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before capturing a stream;
  *   - all calls on a device share the array and it keeps the last call's

@@ -76,9 +76,10 @@ class DeviceLayer:
         pos = np.concatenate([np.arange(L) for L in p.lens]).astype(np.int32)
         for s in range(0, len(seq), chunk):
             x = to_dev(p.x_ctx[s:s + chunk], p.w.dtype, self.device)
+            ws = self._ws("fill", M.mla_compress_workspace_bytes(self.cfg, x.shape[0]))
             M.mla_compress_append(self.cfg, x, self.W["W_DKV"], self.W["W_KR"],
                                   torch.from_numpy(seq[s:s + chunk]).to(self.device),
-                                  torch.from_numpy(pos[s:s + chunk]).to(self.device), self.rope, self.cache)
+                                  torch.from_numpy(pos[s:s + chunk]).to(self.device), self.rope, self.cache, ws=ws)
 
     def fill(self):
         if self.p.w.fill == "direct":
@@ -90,9 +91,24 @@ class DeviceLayer:
     def _ws(self, key, nbytes):
         t = self.ws.get(key)
         if t is None or t.numel() < nbytes:
+            if t is not None:
+                # keep the flags the old workspace collected
+                code, flags = M.mla_get_device_status(t)
+                self.carried_flags = getattr(self, "carried_flags", 0) | flags
             t = M.workspace(nbytes, self.device)
             self.ws[key] = t
         return t
+
+    def status(self, stream=None):
+        """(code, flags) over every workspace this layer's calls used (and clears them): the OR of their
+        status words; code is MLA_ERR_DEVICE_INDEX (5) if any index flag, MLA_ERR_TIMEOUT (4) if any
+        timeout, else 0."""
+        flags = getattr(self, "carried_flags", 0)
+        self.carried_flags = 0
+        for t in self.ws.values():
+            _, f = M.mla_get_device_status(t, stream)
+            flags |= f
+        return (5 if flags & 1 else 4 if flags & 2 else 0), flags
 
     def step(self, x_q=None, stream=None, with_lse=True):
         p, cfg = self.p, self.cfg
@@ -118,6 +134,18 @@ class DeviceLayer:
         return self.o_lat
 
     # ---------------------------------------------------------------- host copies for the oracle
+    def pool_token_bits(self) -> np.ndarray:
+        """Raw bit patterns of the whole pool as [num_blocks, block_size, row] (int16 for bf16, int32 for fp32)."""
+        raw = self.pool.view(torch.int16 if self.p.w.dtype == "bf16" else torch.int32)
+        return raw.cpu().numpy()
+
+    def cache_rows_at(self, seq, pos) -> np.ndarray:
+        """Rows at logical positions pos[i] of sequences seq[i], read back from the pool (float32 numpy)."""
+        bs = self.p.dims.block_size
+        seq, pos = np.asarray(seq, dtype=np.int64), np.asarray(pos, dtype=np.int64)
+        slots = self.p.block_table[seq, pos // bs].astype(np.int64) * bs + pos % bs
+        return self.pool_rows()[torch.from_numpy(slots).to(self.device)].float().cpu().numpy()
+
     def cache_rows_logical(self, b: int, n: int | None = None) -> np.ndarray:
         """Rows 0..n-1 of sequence b read back from the pool, as float32 numpy (exact bf16 values)."""
         p, d = self.p, self.p.dims

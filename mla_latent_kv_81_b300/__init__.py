@@ -9,4 +9,4 @@ from ._binding import (  # noqa: F401
     mla_compress_append_noalloc,
     mla_compress_workspace_bytes, mla_config, mla_decode_attention, mla_decode_workspace_bytes,
     mla_get_device_status, mla_kernel_launches, mla_output_project, mla_output_workspace_bytes, mla_paged_cache,
-    mla_rope_table, mla_rope_table_create, mla_status_string, workspace)
+    mla_rope_table, mla_rope_table_create, mla_selftest_wait_timeout, mla_status_string, workspace)

@@ -58,7 +58,8 @@ def _load():
         "mla_decode_attention": (I, [cfgp, VP, cachep, VP, I, I, VP, VP, VP, Z, VP]),
         "mla_output_workspace_bytes": (Z, [cfgp, I]),
         "mla_output_project": (I, [cfgp, VP, VP, VP, VP, I, VP, Z, VP]),
-        "mla_get_device_status": (I, [VP, P(ctypes.c_uint32)]),
+        "mla_get_device_status": (I, [VP, VP, P(ctypes.c_uint32)]),
+        "mla_selftest_wait_timeout": (I, [VP, Z, ctypes.c_uint32, VP]),
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_kernel_launches": (ctypes.c_uint64, []),
         "mla_compress_append_noalloc": (I, [cfgp, VP, VP, VP, VP, VP, ropep, cachep, I, VP]),
@@ -74,7 +75,7 @@ EXPORTED = ("mla_cache_bytes_per_token", "mla_rope_table_create", "mla_compress_
             "mla_compress_append", "mla_absorb_workspace_bytes", "mla_absorb_query",
             "mla_decode_workspace_bytes", "mla_decode_attention", "mla_output_workspace_bytes",
             "mla_output_project", "mla_get_device_status", "mla_status_string", "mla_kernel_launches",
-            "mla_compress_append_noalloc")
+            "mla_compress_append_noalloc", "mla_selftest_wait_timeout")
 
 
 # ------------------------------------------------------------------ marshalling helpers
@@ -110,8 +111,9 @@ def make_rope(cos_sin) -> mla_rope_table:
 
 
 def workspace(nbytes: int, device):
+    """A caller workspace of at least `nbytes`, zero-filled (its header's status word starts at zero)."""
     import torch
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 # ------------------------------------------------------------------ entry points (same names as the C ABI)
@@ -192,11 +194,18 @@ def mla_output_project(cfg, o_lat, W_UV, W_O, out, ws=None, stream=None):
     return out
 
 
-def mla_get_device_status(stream=None):
-    """Returns (status_code, flags); synchronises the stream."""
+def mla_get_device_status(ws=None, stream=None):
+    """Returns (status_code, flags) of the calls made with workspace `ws` (the library's own word
+    when None), and clears it; synchronises the stream."""
     flags = ctypes.c_uint32(0)
-    code = lib.mla_get_device_status(_stream(stream), ctypes.byref(flags))
+    code = lib.mla_get_device_status(_ptr(ws), _stream(stream), ctypes.byref(flags))
     return int(code), int(flags.value)
+
+
+def mla_selftest_wait_timeout(ws, limit_cycles: int, stream=None):
+    """Run the bounded-wait self-check with workspace `ws` (its status word then reports a timeout)."""
+    _check("mla_selftest_wait_timeout",
+           lib.mla_selftest_wait_timeout(_ptr(ws), ws.numel(), limit_cycles, _stream(stream)))
 
 
 def mla_kernel_launches() -> int:

@@ -12,7 +12,8 @@
 
 namespace mla {
 
-// Device-side error word (bit 0: index skipped, bit 1: bounded wait gave up).
+// Device-side error word of calls that take no workspace (bit 0: index skipped, bit 1: bounded wait
+// gave up).  Calls with a workspace keep their word in the workspace's header instead.
 static __device__ uint32_t g_status_word;
 
 static std::atomic<uint64_t> g_launches{0};
@@ -52,8 +53,10 @@ std::mutex g_dev_mutex;
 uint32_t* g_status_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 
-// Per-device constants, resolved once with that device current.
-mla_status device_ctx(cudaStream_t stream, Ctx* out) {
+// Per-device constants, resolved once with that device current.  Device-side flags of the call go
+// to the status word in the header of `status_ws` (a caller workspace), or to the library's own
+// word when it is null.
+mla_status device_ctx(cudaStream_t stream, void* status_ws, Ctx* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_dev_mutex);
@@ -66,7 +69,7 @@ mla_status device_ctx(cudaStream_t stream, Ctx* out) {
     g_sm_count[dev] = sms;
   }
   out->stream = stream;
-  out->status = g_status_ptr[dev];
+  out->status = status_ws ? static_cast<uint32_t*>(status_ws) : g_status_ptr[dev];
   out->sm_count = g_sm_count[dev];
   out->device = dev;
   return MLA_OK;
@@ -143,9 +146,22 @@ size_t simt_decode_ws(const mla_config* c, int batch, int n_q, int max_blocks, i
 
 int current_sm_count() {
   Ctx ctx;
-  if (device_ctx(nullptr, &ctx) != MLA_OK) return 148;
+  if (device_ctx(nullptr, nullptr, &ctx) != MLA_OK) return 148;
   return ctx.sm_count;
 }
+
+// Every workspace starts with this header; its first word is the status word of the calls that use
+// the workspace.
+constexpr size_t kWsHeader = kWorkspaceHeaderBytes;
+
+// Workspace check shared by every call: at least `need` bytes (header included), 16-byte aligned.
+mla_status check_workspace(const void* ws, size_t bytes, size_t need) {
+  if (need == 0) return MLA_ERR_UNSUPPORTED;
+  if (bytes < need || !ok_ptr(ws)) return MLA_ERR_WORKSPACE;
+  return MLA_OK;
+}
+
+char* ws_body(void* ws) { return static_cast<char*>(ws) + kWsHeader; }
 
 #define MLA_TRY(expr)                    \
   do {                                   \
@@ -158,6 +174,52 @@ int current_sm_count() {
   } while (0)
 
 }  // namespace
+}  // namespace mla
+
+namespace mla {
+
+mla_status validate_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
+                           const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
+                           const mla_paged_cache* cache, int T) {
+  MLA_TRY(check_cfg(cfg));
+  if (T < 0) return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (!ok_ptr(x) || !ok_ptr(W_DKV) || !ok_ptr(W_KR) || !ok_ptr(seq_idx) || !ok_ptr(pos)) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_rope(rope));
+  MLA_TRY(check_cache(cache));
+  if (cfg->dtype == MLA_BF16 && !tc_compress_supported(cfg, T)) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+size_t append_scratch_bytes(const mla_config* cfg, int T) {
+  if (check_cfg(cfg) != MLA_OK || T < 0) return 0;
+  if (cfg->dtype == MLA_BF16) return tc_compress_supported(cfg, T) ? tc_compress_workspace_bytes(cfg, T, current_sm_count()) : 0;
+  return align_up((size_t)T * (cfg->d_c + cfg->d_rope) * sizeof(float), 256);
+}
+
+mla_status run_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
+                      const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
+                      const mla_paged_cache* cache, int T, void* scratch, void* status_ws, cudaStream_t stream) {
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, status_ws, &ctx));
+  if (cfg->dtype == MLA_BF16) {
+    MLA_CUDA(tc_compress_append(ctx, cfg, x, W_DKV, W_KR, seq_idx, pos, *rope, *cache, T, scratch));
+    return MLA_OK;
+  }
+  const int d_c = cfg->d_c, d_r = cfg->d_rope, width = d_c + d_r;
+  float* Y = static_cast<float*>(scratch);
+  GemmDesc g{};
+  g.X = x; g.x_rs = cfg->d_model; g.x_gs = 0; g.x_f32 = 0;
+  g.W = W_DKV; g.w_ms = cfg->d_model; g.w_ks = 1; g.w_gs = 0;
+  g.Y = Y; g.y_rs = width; g.y_gs = 0; g.y_f32 = 1;
+  g.R = T; g.M = d_c; g.K = cfg->d_model; g.G = 1;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
+  g.W = W_KR; g.Y = Y + d_c; g.M = d_r;
+  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
+  MLA_CUDA(simt_compress_epilogue(ctx, cfg->dtype, Y, T, d_c, d_r, seq_idx, pos, *rope, *cache, cfg->block_size));
+  return MLA_OK;
+}
+
 }  // namespace mla
 
 using namespace mla;
@@ -189,59 +251,40 @@ mla_status mla_rope_table_create(const mla_config* cfg, float base, int max_pos,
   MLA_TRY(check_cfg(cfg));
   if (!ok_ptr(d_cos_sin) || max_pos <= 0 || !(base > 1.0f)) return MLA_ERR_INVALID_ARG;
   Ctx ctx;
-  MLA_TRY(device_ctx(stream, &ctx));
+  MLA_TRY(device_ctx(stream, nullptr, &ctx));
   MLA_CUDA(rope_table_fill(ctx, base, max_pos, cfg->d_rope, d_cos_sin));
   return MLA_OK;
 }
 
 size_t mla_compress_workspace_bytes(const mla_config* cfg, int T) {
   if (check_cfg(cfg) != MLA_OK || T < 0) return 0;
-  size_t simt = align_up((size_t)T * (cfg->d_c + cfg->d_rope) * sizeof(float), 256);
-  size_t tc = tc_compress_workspace_bytes(cfg, T);
-  return simt > tc ? simt : tc;
+  if (T == 0) return kWsHeader;
+  const size_t body = append_scratch_bytes(cfg, T);
+  return body ? kWsHeader + body : 0;
 }
 
 mla_status mla_compress_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
                                const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
                                const mla_paged_cache* cache, int T, void* workspace, size_t workspace_bytes,
                                mla_stream_t stream) {
-  MLA_TRY(check_cfg(cfg));
-  if (T < 0) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(validate_append(cfg, x, W_DKV, W_KR, seq_idx, pos, rope, cache, T));
   if (T == 0) return MLA_OK;
-  if (!ok_ptr(x) || !ok_ptr(W_DKV) || !ok_ptr(W_KR) || !ok_ptr(seq_idx) || !ok_ptr(pos)) return MLA_ERR_INVALID_ARG;
-  MLA_TRY(check_rope(rope));
-  MLA_TRY(check_cache(cache));
-  const size_t need = mla_compress_workspace_bytes(cfg, T);
-  if (workspace_bytes < need || (need && !ok_ptr(workspace))) return MLA_ERR_WORKSPACE;
-  Ctx ctx;
-  MLA_TRY(device_ctx(stream, &ctx));
-  if (tc_compress_supported(cfg, T)) {
-    MLA_CUDA(tc_compress_append(ctx, cfg, x, W_DKV, W_KR, seq_idx, pos, *rope, *cache, T, workspace));
-    return MLA_OK;
-  }
-  const int d_c = cfg->d_c, d_r = cfg->d_rope, width = d_c + d_r;
-  float* Y = static_cast<float*>(workspace);
-  GemmDesc g{};
-  g.X = x; g.x_rs = cfg->d_model; g.x_gs = 0; g.x_f32 = 0;
-  g.W = W_DKV; g.w_ms = cfg->d_model; g.w_ks = 1; g.w_gs = 0;
-  g.Y = Y; g.y_rs = width; g.y_gs = 0; g.y_f32 = 1;
-  g.R = T; g.M = d_c; g.K = cfg->d_model; g.G = 1;
-  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
-  g.W = W_KR; g.Y = Y + d_c; g.M = d_r;
-  MLA_CUDA(simt_gemm(ctx, cfg->dtype, g));
-  MLA_CUDA(simt_compress_epilogue(ctx, cfg->dtype, Y, T, d_c, d_r, seq_idx, pos, *rope, *cache, cfg->block_size));
-  return MLA_OK;
+  MLA_TRY(check_workspace(workspace, workspace_bytes, mla_compress_workspace_bytes(cfg, T)));
+  return run_append(cfg, x, W_DKV, W_KR, seq_idx, pos, rope, cache, T, ws_body(workspace), workspace, stream);
 }
 
 size_t mla_absorb_workspace_bytes(const mla_config* cfg, int N) {
   if (check_cfg(cfg) != MLA_OK || N < 0) return 0;
+  if (cfg->dtype == MLA_BF16) {
+    if (N == 0) return kWsHeader;
+    return tc_absorb_supported(cfg, N) ? kWsHeader + tc_absorb_workspace_bytes(cfg, N, current_sm_count()) : 0;
+  }
   const size_t H = cfg->n_heads;
   Carve cv{nullptr};
   cv.take<float>((size_t)N * H * cfg->qk_nope * sizeof(float));
   cv.take<float>((size_t)N * H * cfg->d_rope * sizeof(float));
   cv.take<float>((size_t)N * H * cfg->d_c * sizeof(float));
-  size_t tc = tc_absorb_workspace_bytes(cfg, N);
-  return cv.used > tc ? cv.used : tc;
+  return kWsHeader + cv.used;
 }
 
 mla_status mla_absorb_query(const mla_config* cfg, const void* x, const void* W_Q, const void* W_QR,
@@ -253,16 +296,16 @@ mla_status mla_absorb_query(const mla_config* cfg, const void* x, const void* W_
   if (!ok_ptr(x) || !ok_ptr(W_Q) || !ok_ptr(W_QR) || !ok_ptr(W_UK) || !ok_ptr(q_pos) || !ok_ptr(q_out))
     return MLA_ERR_INVALID_ARG;
   MLA_TRY(check_rope(rope));
-  const size_t need = mla_absorb_workspace_bytes(cfg, N);
-  if (workspace_bytes < need || (need && !ok_ptr(workspace))) return MLA_ERR_WORKSPACE;
+  if (cfg->dtype == MLA_BF16 && !tc_absorb_supported(cfg, N)) return MLA_ERR_UNSUPPORTED;
+  MLA_TRY(check_workspace(workspace, workspace_bytes, mla_absorb_workspace_bytes(cfg, N)));
   Ctx ctx;
-  MLA_TRY(device_ctx(stream, &ctx));
-  if (tc_absorb_supported(cfg, N)) {
-    MLA_CUDA(tc_absorb_query(ctx, cfg, x, W_Q, W_QR, W_UK, q_pos, *rope, q_out, N, workspace));
+  MLA_TRY(device_ctx(stream, workspace, &ctx));
+  if (cfg->dtype == MLA_BF16) {
+    MLA_CUDA(tc_absorb_query(ctx, cfg, x, W_Q, W_QR, W_UK, q_pos, *rope, q_out, N, ws_body(workspace)));
     return MLA_OK;
   }
   const int H = cfg->n_heads, qn = cfg->qk_nope, d_r = cfg->d_rope, d_c = cfg->d_c;
-  Carve cv{static_cast<char*>(workspace)};
+  Carve cv{ws_body(workspace)};
   float* Yn = cv.take<float>((size_t)N * H * qn * sizeof(float));
   float* Yr = cv.take<float>((size_t)N * H * d_r * sizeof(float));
   float* Ya = cv.take<float>((size_t)N * H * d_c * sizeof(float));
@@ -288,10 +331,13 @@ mla_status mla_absorb_query(const mla_config* cfg, const void* x, const void* W_
 
 size_t mla_decode_workspace_bytes(const mla_config* cfg, int batch, int n_q, int max_blocks_per_seq) {
   if (check_cfg(cfg) != MLA_OK || batch < 0 || n_q <= 0 || max_blocks_per_seq <= 0) return 0;
+  if (batch == 0) return kWsHeader;
   const int sms = current_sm_count();
-  size_t simt = simt_decode_ws(cfg, batch, n_q, max_blocks_per_seq, sms);
-  size_t tc = tc_decode_workspace_bytes(cfg, batch, n_q, max_blocks_per_seq, sms);
-  return simt > tc ? simt : tc;
+  if (cfg->dtype == MLA_BF16) {
+    if (!tc_decode_supported(cfg, batch, n_q)) return 0;
+    return kWsHeader + tc_decode_workspace_bytes(cfg, batch, n_q, max_blocks_per_seq, sms);
+  }
+  return kWsHeader + simt_decode_ws(cfg, batch, n_q, max_blocks_per_seq, sms);
 }
 
 mla_status mla_decode_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache,
@@ -303,19 +349,20 @@ mla_status mla_decode_attention(const mla_config* cfg, const void* q, const mla_
   if (!ok_ptr(q) || !ok_ptr(kv_len) || !ok_ptr(o_lat) || (lse && !aligned16(lse))) return MLA_ERR_INVALID_ARG;
   MLA_TRY(check_cache(cache));
   if (cache->batch < batch) return MLA_ERR_INVALID_ARG;
-  const size_t need = mla_decode_workspace_bytes(cfg, batch, n_q, cache->max_blocks_per_seq);
-  if (workspace_bytes < need || (need && !ok_ptr(workspace))) return MLA_ERR_WORKSPACE;
+  if (cfg->dtype == MLA_BF16 && !tc_decode_supported(cfg, batch, n_q)) return MLA_ERR_UNSUPPORTED;
+  MLA_TRY(check_workspace(workspace, workspace_bytes,
+                          mla_decode_workspace_bytes(cfg, batch, n_q, cache->max_blocks_per_seq)));
   Ctx ctx;
-  MLA_TRY(device_ctx(stream, &ctx));
+  MLA_TRY(device_ctx(stream, workspace, &ctx));
   const float scale = resolve_scale(cfg);
-  if (tc_decode_supported(cfg, batch, n_q)) {
-    MLA_CUDA(tc_decode_attention(ctx, cfg, q, *cache, kv_len, batch, n_q, scale, o_lat, lse, workspace));
+  if (cfg->dtype == MLA_BF16) {
+    MLA_CUDA(tc_decode_attention(ctx, cfg, q, *cache, kv_len, batch, n_q, scale, o_lat, lse, ws_body(workspace)));
     return MLA_OK;
   }
   int splits = 1, tps = 0;
   simt_split_plan(cfg, batch, n_q, cache->max_blocks_per_seq, ctx.sm_count, &splits, &tps);
   const size_t items = (size_t)batch * n_q;
-  Carve cv{static_cast<char*>(workspace)};
+  Carve cv{ws_body(workspace)};
   float* part_o = nullptr;
   float* part_lse = nullptr;
   if (splits > 1) {
@@ -332,9 +379,11 @@ mla_status mla_decode_attention(const mla_config* cfg, const void* q, const mla_
 
 size_t mla_output_workspace_bytes(const mla_config* cfg, int N) {
   if (check_cfg(cfg) != MLA_OK || N < 0) return 0;
-  size_t simt = align_up((size_t)N * cfg->n_heads * cfg->v_head * sizeof(float), 256);
-  size_t tc = tc_output_workspace_bytes(cfg, N);
-  return simt > tc ? simt : tc;
+  if (cfg->dtype == MLA_BF16) {
+    if (N == 0) return kWsHeader;
+    return tc_output_supported(cfg, N) ? kWsHeader + tc_output_workspace_bytes(cfg, N, current_sm_count()) : 0;
+  }
+  return kWsHeader + align_up((size_t)N * cfg->n_heads * cfg->v_head * sizeof(float), 256);
 }
 
 mla_status mla_output_project(const mla_config* cfg, const void* o_lat, const void* W_UV, const void* W_O, void* out,
@@ -343,16 +392,16 @@ mla_status mla_output_project(const mla_config* cfg, const void* o_lat, const vo
   if (N < 0) return MLA_ERR_INVALID_ARG;
   if (N == 0) return MLA_OK;
   if (!ok_ptr(o_lat) || !ok_ptr(W_UV) || !ok_ptr(W_O) || !ok_ptr(out)) return MLA_ERR_INVALID_ARG;
-  const size_t need = mla_output_workspace_bytes(cfg, N);
-  if (workspace_bytes < need || (need && !ok_ptr(workspace))) return MLA_ERR_WORKSPACE;
+  if (cfg->dtype == MLA_BF16 && !tc_output_supported(cfg, N)) return MLA_ERR_UNSUPPORTED;
+  MLA_TRY(check_workspace(workspace, workspace_bytes, mla_output_workspace_bytes(cfg, N)));
   Ctx ctx;
-  MLA_TRY(device_ctx(stream, &ctx));
-  if (tc_output_supported(cfg, N)) {
-    MLA_CUDA(tc_output_project(ctx, cfg, o_lat, W_UV, W_O, out, N, workspace));
+  MLA_TRY(device_ctx(stream, workspace, &ctx));
+  if (cfg->dtype == MLA_BF16) {
+    MLA_CUDA(tc_output_project(ctx, cfg, o_lat, W_UV, W_O, out, N, ws_body(workspace)));
     return MLA_OK;
   }
   const int H = cfg->n_heads, v = cfg->v_head, d_c = cfg->d_c;
-  float* Yo = static_cast<float*>(workspace);
+  float* Yo = reinterpret_cast<float*>(ws_body(workspace));
   // o^h[v] = sum_c W_UV[h][v][c] o_lat^h[c]   (batched over heads)
   GemmDesc a{};
   a.X = o_lat; a.x_rs = (long long)H * d_c; a.x_gs = d_c; a.x_f32 = 0;
@@ -370,17 +419,27 @@ mla_status mla_output_project(const mla_config* cfg, const void* o_lat, const vo
   return MLA_OK;
 }
 
-mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags) {
+mla_status mla_get_device_status(const void* workspace, mla_stream_t stream, uint32_t* flags) {
+  if (workspace && !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   Ctx ctx;
-  MLA_TRY(device_ctx(stream, &ctx));
-  MLA_CUDA(cudaStreamSynchronize(stream));
+  MLA_TRY(device_ctx(stream, const_cast<void*>(workspace), &ctx));
   uint32_t word = 0;
-  MLA_CUDA(cudaMemcpy(&word, ctx.status, sizeof(word), cudaMemcpyDeviceToHost));
-  const uint32_t zero = 0;
-  MLA_CUDA(cudaMemcpy(ctx.status, &zero, sizeof(zero), cudaMemcpyHostToDevice));
+  MLA_CUDA(cudaMemcpyAsync(&word, ctx.status, sizeof(word), cudaMemcpyDeviceToHost, stream));
+  MLA_CUDA(cudaMemsetAsync(ctx.status, 0, sizeof(uint32_t), stream));
+  MLA_CUDA(cudaStreamSynchronize(stream));
   if (flags) *flags = word;
   if (word & kFlagIndex) return MLA_ERR_DEVICE_INDEX;
   if (word & kFlagTimeout) return MLA_ERR_TIMEOUT;
+  return MLA_OK;
+}
+
+mla_status mla_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_cycles,
+                                     mla_stream_t stream) {
+  if (limit_cycles < 10000u || limit_cycles > 200000000u) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_workspace(workspace, workspace_bytes, kWsHeader));
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, workspace, &ctx));
+  MLA_CUDA(launch_wait_timeout_check(ctx, (long long)limit_cycles));
   return MLA_OK;
 }
 

@@ -11,6 +11,10 @@ namespace mla {
 
 enum : uint32_t { kFlagIndex = 1u, kFlagTimeout = 2u };
 
+// Every caller workspace starts with a header of this many bytes; its first 32-bit word is the
+// device status word of the calls that use the workspace.
+constexpr size_t kWorkspaceHeaderBytes = 256;
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -46,10 +50,23 @@ __device__ __forceinline__ long long cache_row(const int32_t* table, int max_blo
 // ------------------------------------------------------------------ launch plumbing
 struct Ctx {
   cudaStream_t stream;
-  uint32_t* status;   // device error word of the current device
+  uint32_t* status;   // device error word of this call (its workspace header, or the library's word)
   int sm_count;
   int device;
 };
+
+// Argument checks of the cache append shared by the allocating and the allocation-free entry points,
+// in the order they are applied (no workspace check).
+mla_status validate_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
+                           const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
+                           const mla_paged_cache* cache, int T);
+// Scratch bytes the append of T tokens needs beyond the workspace header (0: unsupported).
+size_t append_scratch_bytes(const mla_config* cfg, int T);
+// The append after validation: `scratch` holds append_scratch_bytes(cfg, T) bytes; device-side
+// flags go to the status word in the header of `status_ws`, or to the library's word when null.
+mla_status run_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
+                      const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
+                      const mla_paged_cache* cache, int T, void* scratch, void* status_ws, cudaStream_t stream);
 
 // Generic strided GEMM description: Y[g][r][m] = sum_k X[g][r][k] * W[g][m][k]
 // where W is addressed as W + g*w_gs + m*w_ms + k*w_ks (so both [m][k] and

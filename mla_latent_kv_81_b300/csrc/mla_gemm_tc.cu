@@ -446,16 +446,16 @@ bool tc_compress_supported(const mla_config* cfg, int T) {
   return shapes_ok(cfg) && T > 0 && stack_ok(cfg->d_c) && (cfg->d_c + cfg->d_rope) % 4 == 0;
 }
 
-size_t tc_compress_workspace_bytes(const mla_config* cfg, int T) {
+size_t tc_compress_workspace_bytes(const mla_config* cfg, int T, int sm_count) {
   if (!tc_compress_supported(cfg, T)) return 0;
-  return align256(partial_bytes(plan_stacked(cfg->d_c, cfg->d_rope, T, cfg->d_model, 148)));
+  return align256(partial_bytes(plan_stacked(cfg->d_c, cfg->d_rope, T, cfg->d_model, sm_count)));
 }
 
 cudaError_t tc_compress_append(const Ctx& ctx, const mla_config* cfg, const void* x, const void* W_DKV,
                                const void* W_KR, const int32_t* seq_idx, const int32_t* pos,
                                const mla_rope_table& rope, const mla_paged_cache& cache, int T, void* workspace) {
   const int D = cfg->d_model, d_c = cfg->d_c, d_r = cfg->d_rope;
-  GemmPlan pl = plan_stacked(d_c, d_r, T, D, 148);
+  GemmPlan pl = plan_stacked(d_c, d_r, T, D, ctx.sm_count);
   pl.args.partial = static_cast<float*>(workspace);
   CUtensorMap a1, a2, b;
   if (!make_map(&a1, W_DKV, D, d_c, 1, (uint64_t)D * 2, (uint64_t)D * 2 * d_c, 128) ||
@@ -484,12 +484,12 @@ struct AbsorbLayout {
   GemmPlan pqr, pa;
   size_t off_nope, total;
 };
-AbsorbLayout absorb_layout(const mla_config* cfg, int N) {
+AbsorbLayout absorb_layout(const mla_config* cfg, int N, int sm_count) {
   AbsorbLayout l;
   const int H = cfg->n_heads;
-  l.pqr = plan_stacked(H * cfg->qk_nope, H * cfg->d_rope, N, cfg->d_model, 148);
+  l.pqr = plan_stacked(H * cfg->qk_nope, H * cfg->d_rope, N, cfg->d_model, sm_count);
   // K = 2 * qk_nope: the same W_UK^T tile multiplies the high and low bf16 parts of q_nope
-  l.pa = plan_gemm(cfg->d_c, N, 2 * cfg->qk_nope, H, true, true, 148);
+  l.pa = plan_gemm(cfg->d_c, N, 2 * cfg->qk_nope, H, true, true, sm_count);
   l.pa.args.a_k_period = cfg->qk_nope;
   l.off_nope = align256(partial_bytes(l.pqr));
   l.total = l.off_nope + align256((size_t)N * H * cfg->qk_nope * 2 * 2);
@@ -497,16 +497,16 @@ AbsorbLayout absorb_layout(const mla_config* cfg, int N) {
 }
 }  // namespace
 
-size_t tc_absorb_workspace_bytes(const mla_config* cfg, int N) {
+size_t tc_absorb_workspace_bytes(const mla_config* cfg, int N, int sm_count) {
   if (!tc_absorb_supported(cfg, N)) return 0;
-  return absorb_layout(cfg, N).total;
+  return absorb_layout(cfg, N, sm_count).total;
 }
 
 cudaError_t tc_absorb_query(const Ctx& ctx, const mla_config* cfg, const void* x, const void* W_Q, const void* W_QR,
                             const void* W_UK, const int32_t* q_pos, const mla_rope_table& rope, void* q_out, int N,
                             void* workspace) {
   const int D = cfg->d_model, H = cfg->n_heads, qk = cfg->qk_nope, d_r = cfg->d_rope, d_c = cfg->d_c;
-  AbsorbLayout l = absorb_layout(cfg, N);
+  AbsorbLayout l = absorb_layout(cfg, N, ctx.sm_count);
   char* ws = static_cast<char*>(workspace);
   l.pqr.args.partial = reinterpret_cast<float*>(ws);
   bf16* q_nope = reinterpret_cast<bf16*>(ws + l.off_nope);
@@ -544,11 +544,11 @@ struct OutputLayout {
   GemmPlan pv, po;
   size_t off_o, off_part, total;
 };
-OutputLayout output_layout(const mla_config* cfg, int N) {
+OutputLayout output_layout(const mla_config* cfg, int N, int sm_count) {
   OutputLayout l;
   const int H = cfg->n_heads;
-  l.pv = plan_gemm(cfg->v_head, N, cfg->d_c, H, false, true, 148);
-  l.po = plan_gemm(cfg->d_model, N, H * cfg->v_head, 1, false, false, 148);
+  l.pv = plan_gemm(cfg->v_head, N, cfg->d_c, H, false, true, sm_count);
+  l.po = plan_gemm(cfg->d_model, N, H * cfg->v_head, 1, false, false, sm_count);
   l.off_o = 0;
   l.off_part = align256((size_t)N * H * cfg->v_head * 2);
   l.total = l.off_part + align256(partial_bytes(l.po));
@@ -556,15 +556,15 @@ OutputLayout output_layout(const mla_config* cfg, int N) {
 }
 }  // namespace
 
-size_t tc_output_workspace_bytes(const mla_config* cfg, int N) {
+size_t tc_output_workspace_bytes(const mla_config* cfg, int N, int sm_count) {
   if (!tc_output_supported(cfg, N)) return 0;
-  return output_layout(cfg, N).total;
+  return output_layout(cfg, N, sm_count).total;
 }
 
 cudaError_t tc_output_project(const Ctx& ctx, const mla_config* cfg, const void* o_lat, const void* W_UV,
                               const void* W_O, void* out, int N, void* workspace) {
   const int D = cfg->d_model, H = cfg->n_heads, v = cfg->v_head, d_c = cfg->d_c;
-  OutputLayout l = output_layout(cfg, N);
+  OutputLayout l = output_layout(cfg, N, ctx.sm_count);
   char* ws = static_cast<char*>(workspace);
   bf16* o = reinterpret_cast<bf16*>(ws + l.off_o);
   l.po.args.partial = reinterpret_cast<float*>(ws + l.off_part);

@@ -40,15 +40,17 @@ extern "C" mla_status mla_compress_append_noalloc(const mla_config* cfg, const v
                                                   const void* W_KR, const int32_t* seq_idx, const int32_t* pos,
                                                   const mla_rope_table* rope, const mla_paged_cache* cache, int T,
                                                   mla_stream_t stream) {
-  if (mla_cache_bytes_per_token(cfg) == 0 || T < 0) return MLA_ERR_INVALID_ARG;
-  if (T == 0) return MLA_OK;
-  // The scratch this call would need must fit in the fixed array; larger calls are refused
-  // before anything touches the GPU.
-  if (mla_compress_workspace_bytes(cfg, T) > kScratchBytes) return MLA_ERR_WORKSPACE;
+  // the same argument checks as mla_compress_append, in the same order
+  const mla_status v = mla::validate_append(cfg, x, W_DKV, W_KR, seq_idx, pos, rope, cache, T);
+  if (v != MLA_OK || T == 0) return v;
+  // the scratch this call would need must fit in the fixed array; larger calls are refused before
+  // anything touches the GPU
+  if (mla::append_scratch_bytes(cfg, T) > kScratchBytes) return MLA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const mla_status s = scratch_on_current_device(&scratch);
   if (s != MLA_OK) return s;
-  // Every scratch element the kernels read is written earlier in the same call, so the array
-  // needs no clearing between calls.
-  return mla_compress_append(cfg, x, W_DKV, W_KR, seq_idx, pos, rope, cache, T, scratch, kScratchBytes, stream);
+  // Every scratch element the kernels read is written earlier in the same call, so the array needs
+  // no clearing between calls.  Device-side flags go to the library's own status word (read with
+  // mla_get_device_status(NULL, ...)): there is no caller workspace to hold them.
+  return mla::run_append(cfg, x, W_DKV, W_KR, seq_idx, pos, rope, cache, T, scratch, nullptr, stream);
 }

@@ -1,9 +1,9 @@
 // General SIMT (CUDA-core, fp32 arithmetic) kernels for every MLA decode step.
 //
-// These serve any layer shape and both storage types.  They are the fp32 path
-// (tensor cores cannot hold fp32 operands at fp32 accuracy) and the fallback
-// for bf16 shapes the tcgen05 kernels do not specialise.  The math of each
-// step is documented in include/mla.h.
+// These serve fp32 storage at any layer shape: tensor cores cannot hold fp32
+// operands at fp32 accuracy.  bf16 storage runs only on the tcgen05 kernels
+// (mla_decode_tc.cu, mla_gemm_tc.cu); these entry points refuse it.  The math
+// of each step is documented in include/mla.h.
 #include <math.h>
 
 #include "mla_common.cuh"
@@ -278,20 +278,17 @@ __global__ void rope_table_kernel(double base, int max_pos, int d_rope, float* c
 }  // namespace
 
 cudaError_t simt_gemm(const Ctx& c, int dtype, const GemmDesc& d) {
+  if (dtype != MLA_F32) return cudaErrorNotSupported;
   if (d.R == 0 || d.M == 0 || d.G == 0) return cudaSuccess;
-  return dtype == MLA_BF16 ? gemm_typed<bf16>(c, d) : gemm_typed<float>(c, d);
+  return gemm_typed<float>(c, d);
 }
 
 cudaError_t simt_compress_epilogue(const Ctx& c, int dtype, const float* Y, int T_, int d_c, int d_r,
                                    const int32_t* seq_idx, const int32_t* pos, const mla_rope_table& rope,
                                    const mla_paged_cache& cache, int block_size) {
+  if (dtype != MLA_F32) return cudaErrorNotSupported;
   if (T_ == 0) return cudaSuccess;
-  if (dtype == MLA_BF16)
-    compress_epilogue_kernel<bf16><<<T_, 128, 0, c.stream>>>(Y, T_, d_c, d_r, seq_idx, pos, rope.cos_sin, rope.max_pos,
-                                                             (bf16*)cache.pool, cache.num_blocks, cache.block_table,
-                                                             cache.max_blocks_per_seq, cache.batch, block_size, c.status);
-  else
-    compress_epilogue_kernel<float><<<T_, 128, 0, c.stream>>>(Y, T_, d_c, d_r, seq_idx, pos, rope.cos_sin, rope.max_pos,
+  compress_epilogue_kernel<float><<<T_, 128, 0, c.stream>>>(Y, T_, d_c, d_r, seq_idx, pos, rope.cos_sin, rope.max_pos,
                                                               (float*)cache.pool, cache.num_blocks, cache.block_table,
                                                               cache.max_blocks_per_seq, cache.batch, block_size, c.status);
   count_launch();
@@ -300,13 +297,10 @@ cudaError_t simt_compress_epilogue(const Ctx& c, int dtype, const float* Y, int 
 
 cudaError_t simt_query_epilogue(const Ctx& c, int dtype, const float* Y_abs, const float* Y_rope, int N, int H,
                                 int d_c, int d_r, const int32_t* q_pos, const mla_rope_table& rope, void* q_out) {
+  if (dtype != MLA_F32) return cudaErrorNotSupported;
   if (N == 0) return cudaSuccess;
   dim3 grid(N, H);
-  if (dtype == MLA_BF16)
-    query_epilogue_kernel<bf16><<<grid, 128, 0, c.stream>>>(Y_abs, Y_rope, H, d_c, d_r, q_pos, rope.cos_sin,
-                                                            rope.max_pos, (bf16*)q_out, c.status);
-  else
-    query_epilogue_kernel<float><<<grid, 128, 0, c.stream>>>(Y_abs, Y_rope, H, d_c, d_r, q_pos, rope.cos_sin,
+  query_epilogue_kernel<float><<<grid, 128, 0, c.stream>>>(Y_abs, Y_rope, H, d_c, d_r, q_pos, rope.cos_sin,
                                                              rope.max_pos, (float*)q_out, c.status);
   count_launch();
   return cudaGetLastError();
@@ -315,20 +309,13 @@ cudaError_t simt_query_epilogue(const Ctx& c, int dtype, const float* Y_abs, con
 cudaError_t simt_decode(const Ctx& c, int dtype, const void* q, const mla_paged_cache& cache, int block_size,
                         const int32_t* kv_len, int B, int n_q, int H, int d_c, int d_r, float scale, int splits,
                         int tokens_per_split, float* part_o, float* part_lse, void* o_lat, float* lse_out) {
+  if (dtype != MLA_F32) return cudaErrorNotSupported;
   if (B == 0) return cudaSuccess;
   const int width = d_c + d_r;
   const size_t smem = sizeof(float) * (kHeadsPerCta * width + kChunk * (width + 1));
   dim3 grid(B * n_q, (H + kHeadsPerCta - 1) / kHeadsPerCta, splits);
   const float scale_log2 = scale * kLog2e;
-  if (dtype == MLA_BF16) {
-    auto k = simt_decode_kernel<bf16>;
-    const cudaError_t ea = ensure_smem_limit((const void*)k, (int)smem, c.device);
-    if (ea != cudaSuccess) return ea;
-    k<<<grid, 128, smem, c.stream>>>((const bf16*)q, (const bf16*)cache.pool, cache.block_table,
-                                     cache.max_blocks_per_seq, cache.num_blocks, block_size, kv_len, n_q, H, d_c, d_r,
-                                     scale_log2, splits, tokens_per_split, part_o, part_lse, (bf16*)o_lat, lse_out,
-                                     c.status);
-  } else {
+  {
     auto k = simt_decode_kernel<float>;
     const cudaError_t ea = ensure_smem_limit((const void*)k, (int)smem, c.device);
     if (ea != cudaSuccess) return ea;
@@ -343,12 +330,10 @@ cudaError_t simt_decode(const Ctx& c, int dtype, const void* q, const mla_paged_
 
 cudaError_t combine_partials(const Ctx& c, int dtype, const float* part_o, const float* part_lse, int items,
                              int splits, int H, int d_c, void* o_lat, float* lse_out) {
+  if (dtype != MLA_F32) return cudaErrorNotSupported;
   if (items == 0) return cudaSuccess;
   dim3 grid(items, H);
-  if (dtype == MLA_BF16)
-    combine_kernel<bf16><<<grid, 128, 0, c.stream>>>(part_o, part_lse, splits, H, d_c, (bf16*)o_lat, lse_out);
-  else
-    combine_kernel<float><<<grid, 128, 0, c.stream>>>(part_o, part_lse, splits, H, d_c, (float*)o_lat, lse_out);
+  combine_kernel<float><<<grid, 128, 0, c.stream>>>(part_o, part_lse, splits, H, d_c, (float*)o_lat, lse_out);
   count_launch();
   return cudaGetLastError();
 }

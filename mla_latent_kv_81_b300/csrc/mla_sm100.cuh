@@ -99,24 +99,29 @@ __device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity, u
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Gives up after
-// kTimeoutCycles: sets the timeout flag in the device status word and the
-// CTA's abort flag, and returns false.  Also returns false as soon as another
-// thread of the CTA has aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                          volatile int* abort_flag) {
+// Wait for the phase with the given parity to complete.  Gives up after `limit` SM cycles: sets the
+// timeout flag in the device status word and the CTA's abort flag, and returns false.  Also returns
+// false as soon as another thread of the CTA has aborted.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                volatile int* abort_flag, long long limit) {
   const uint32_t a = smem_u32(bar);
   if (mbar_test(a, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_test_sleep(a, parity, 100000u)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       atomicOr(status, kFlagTimeout);
       *abort_flag = 1;
       return false;
     }
   }
+}
+
+// The kernels' wait: gives up after kTimeoutCycles (~2 s).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          volatile int* abort_flag) {
+  return mbar_wait_limit(bar, parity, status, abort_flag, kTimeoutCycles);
 }
 
 // Variants for barriers that only this CTA's threads, its TMA loads and its tcgen05 commits complete:

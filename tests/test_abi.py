@@ -55,14 +55,54 @@ def test_invalid_config_is_rejected():
     assert M.mla_compress_workspace_bytes(cfg, 4) == 0
 
 
-def test_workspace_sizes_cover_the_fp32_intermediates():
+def test_workspace_sizes_cover_the_header_and_the_fp32_intermediates():
     for dims, dtype in ((I.TINY, "f32"), (I.DSV2, "bf16")):
         cfg = M.make_config(dims, dtype)
-        assert M.mla_compress_workspace_bytes(cfg, 100) >= 100 * dims.row * 4
+        assert M.mla_compress_workspace_bytes(cfg, 100) >= 256 + 100 * dims.row * 4
         H = dims.n_heads
-        assert M.mla_absorb_workspace_bytes(cfg, 10) >= 10 * H * (dims.qk_nope + dims.d_rope + dims.d_c) * 4
-        assert M.mla_output_workspace_bytes(cfg, 10) >= 10 * H * dims.v_head * 4
-        assert M.mla_decode_workspace_bytes(cfg, 4, 1, 1024) >= 0
+        assert M.mla_absorb_workspace_bytes(cfg, 10) >= 256 + 10 * H * dims.qk_nope * 4
+        assert M.mla_output_workspace_bytes(cfg, 10) >= 256 + 10 * H * dims.v_head * 2
+        assert M.mla_decode_workspace_bytes(cfg, 4, 1, 1024) >= 256
+        # every workspace, even for zero work, holds at least the status header
+        assert M.mla_compress_workspace_bytes(cfg, 0) == 256
+        assert M.mla_decode_workspace_bytes(cfg, 0, 1, 1) == 256
+
+
+def test_bf16_shapes_outside_the_tensor_core_kernels_are_refused_on_the_host():
+    """bf16 runs only on the tcgen05 kernels: a bf16 layer with 16 heads gets MLA_ERR_UNSUPPORTED from
+    every entry point (after the pointer checks, before any device work) and a zero workspace size."""
+    lib, byref = M.lib, ctypes.byref
+    dims = I.Dims(d_model=256, n_heads=16, qk_nope=32, d_rope=32, v_head=48, d_c=256)
+    cfg = M.make_config(dims, "bf16")
+    UNS = 2
+    assert M.mla_decode_workspace_bytes(cfg, 2, 1, 4) == 0
+    assert M.mla_absorb_workspace_bytes(cfg, 2) == 0
+    assert M.mla_output_workspace_bytes(cfg, 2) == 0
+    assert M.mla_compress_workspace_bytes(cfg, 2) == 0
+    rope = M.mla_rope_table(0x1000, 16)
+    cache = M.mla_paged_cache(0x2000, 4, 0x3000, 2, 2)
+    assert lib.mla_decode_attention(byref(cfg), _fake(1), byref(cache), _fake(2), 2, 1, _fake(3), None, _fake(4),
+                                    1 << 30, None) == UNS
+    assert lib.mla_absorb_query(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope), _fake(6), 2,
+                                _fake(7), 1 << 30, None) == UNS
+    assert lib.mla_output_project(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), 2, _fake(6), 1 << 30,
+                                  None) == UNS
+    assert lib.mla_compress_append(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope),
+                                   byref(cache), 2, _fake(6), 1 << 30, None) == UNS
+    assert lib.mla_compress_append_noalloc(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5),
+                                           byref(rope), byref(cache), 2, None) == UNS
+    # the same shape in fp32 is supported (CUDA-core kernels)
+    assert M.mla_decode_workspace_bytes(M.make_config(dims, "f32"), 2, 1, 4) >= 256
+
+
+def test_wait_timeout_selftest_rejects_long_limits_on_the_host():
+    """The failure-detection self-check only accepts short limits (at most ~0.1 s of SM cycles) and a
+    workspace holding the status header."""
+    lib = M.lib
+    assert lib.mla_selftest_wait_timeout(_fake(1), 256, 5000, None) == 1
+    assert lib.mla_selftest_wait_timeout(_fake(1), 256, 400_000_000, None) == 1
+    assert lib.mla_selftest_wait_timeout(None, 256, 2_000_000, None) == 6
+    assert lib.mla_selftest_wait_timeout(_fake(1), 16, 2_000_000, None) == 6
 
 
 def _fake(n):
@@ -87,9 +127,13 @@ def test_bad_arguments_fail_before_any_launch():
                                    byref(cache), -1, _fake(6), 1 << 20, None) == INV
     # zero tokens is a no-op even with null pointers
     assert lib.mla_compress_append(byref(cfg), None, None, None, None, None, None, None, 0, None, 0, None) == 0
-    # workspace too small
+    # workspace too small, or null
     assert lib.mla_compress_append(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope),
                                    byref(cache), 8, _fake(6), 16, None) == WS
+    assert lib.mla_compress_append(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope),
+                                   byref(cache), 8, None, 1 << 20, None) == WS
+    # misaligned workspace passed to the status read
+    assert lib.mla_get_device_status(ctypes.c_void_p(0x10008), None, None) == INV
     # empty cache description
     bad_cache = M.mla_paged_cache(0x2000, 0, 0x3000, 2, 1)
     assert lib.mla_compress_append(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope),

@@ -1,7 +1,8 @@
 """mla_compress_append_noalloc: the cache append for callers that cannot allocate device memory.
 
-It keeps its scratch in a fixed array inside the library instead of a caller-provided
-workspace, so it must write the same cache rows as the allocating mla_compress_append."""
+It keeps its scratch in a fixed array inside the library instead of a caller-provided workspace,
+and runs the same kernels with the same split plan as the allocating mla_compress_append, so it
+must write bit-identical cache rows."""
 import ctypes
 
 import numpy as np
@@ -11,17 +12,25 @@ import torch
 import mla_harness as Hn
 import mla_inputs as I
 import mla_latent_kv_81_b300 as M
-from gpu_helpers import assert_close
 
 SCRATCH_BYTES = 16 << 20
+HEADER_BYTES = 256
+
+
+def test_noalloc_scratch_covers_every_call_up_to_1024_tokens():
+    """No GPU needed: the split plan is not monotone in T, so check every token count the documented
+    promise covers, not only the largest."""
+    cfg = M.make_config(I.DSV2, "bf16")
+    for T in range(1, 1025):
+        assert M.mla_compress_workspace_bytes(cfg, T) - HEADER_BYTES <= SCRATCH_BYTES, T
 
 
 def test_noalloc_refuses_calls_larger_than_its_scratch():
-    """No GPU needed: a call whose scratch exceeds the fixed 16 MiB is refused before any device work."""
+    """No GPU needed: a call whose scratch exceeds the fixed 16 MiB is refused before any device work,
+    after the same argument checks as mla_compress_append."""
     cfg = M.make_config(I.DSV2, "bf16")
-    assert M.mla_compress_workspace_bytes(cfg, 1024) <= SCRATCH_BYTES
     T = 65536
-    assert M.mla_compress_workspace_bytes(cfg, T) > SCRATCH_BYTES
+    assert M.mla_compress_workspace_bytes(cfg, T) - HEADER_BYTES > SCRATCH_BYTES
     rope = M.mla_rope_table(0x1000, 16)
     cache = M.mla_paged_cache(0x2000, 4, 0x3000, 2, 1)
     fake = [ctypes.c_void_p(0x10000 * i) for i in range(1, 6)]
@@ -30,6 +39,12 @@ def test_noalloc_refuses_calls_larger_than_its_scratch():
     assert M.mla_status_string(code) == M.mla_status_string(6)   # MLA_ERR_WORKSPACE
     assert code == 6
     assert M.lib.mla_compress_append_noalloc(None, *fake, ctypes.byref(rope), ctypes.byref(cache), 4, None) == 1
+    # a bad pointer is reported as such even when the call is also too large (same checks, same order)
+    bad = [None] + fake[1:]
+    assert M.lib.mla_compress_append_noalloc(ctypes.byref(cfg), *bad, ctypes.byref(rope), ctypes.byref(cache), T,
+                                             None) == 1
+    assert M.lib.mla_compress_append(ctypes.byref(cfg), *bad, ctypes.byref(rope), ctypes.byref(cache), T, None, 0,
+                                     None) == 1
 
 
 @pytest.mark.gpu
@@ -48,15 +63,15 @@ def test_noalloc_append_matches_the_allocating_append_on_two_calls():
         seq, pos = np.ascontiguousarray(pick[:, 0]), np.ascontiguousarray(pick[:, 1])
         x = Hn.to_dev(I.draw_hidden(rng, T, dims.d_model, "bf16"), "bf16")
         s_dev, p_dev = torch.from_numpy(seq).cuda(), torch.from_numpy(pos).cuda()
-        M.mla_compress_append(ref.cfg, x, ref.W["W_DKV"], ref.W["W_KR"], s_dev, p_dev, ref.rope, ref.cache)
+        ws = M.workspace(M.mla_compress_workspace_bytes(ref.cfg, T), "cuda")
+        M.mla_compress_append(ref.cfg, x, ref.W["W_DKV"], ref.W["W_KR"], s_dev, p_dev, ref.rope, ref.cache, ws=ws)
         M.mla_compress_append_noalloc(got.cfg, x, got.W["W_DKV"], got.W["W_KR"], s_dev, p_dev, got.rope, got.cache)
-        code, flags = M.mla_get_device_status()
+        code, flags = M.mla_get_device_status(ws)
         assert code == 0, (M.mla_status_string(code), flags)
-        rows = np.concatenate([I.paged_slots(p.block_table, int(b), [int(q)], dims.block_size) for b, q in pick])
-        idx = torch.from_numpy(rows).cuda()
-        r_ref = ref.pool_rows()[idx].float().cpu().numpy()
-        r_got = got.pool_rows()[idx].float().cpu().numpy()
+        code, flags = M.mla_get_device_status(None)   # the allocation-free call's flags
+        assert code == 0, (M.mla_status_string(code), flags)
+        # the same kernels with the same plan: the whole pool must be bit-identical, written rows and
+        # untouched NaN sentinels alike
+        assert torch.equal(ref.pool.view(torch.int16), got.pool.view(torch.int16)), f"call {call}"
+        r_got = got.cache_rows_at(seq, pos)
         assert np.isfinite(r_got).all()
-        assert_close(r_got, r_ref, "bf16", f"call {call}")
-        # rows no token addressed keep their NaN sentinel in both pools
-        assert torch.equal(torch.isnan(ref.pool), torch.isnan(got.pool))
