@@ -89,11 +89,16 @@ typedef struct {
   int dtype;           /* mla_dtype */
 } mla_config;
 
-/* Paged latent cache.  pool: [num_blocks][block_size][d_c + d_rope] of dtype,
- * each row = [c_KV || k_R] ([ZQ "What MLA caches..."]: the latent is the only
- * content written to the cache; [SC]: plus the small positional component).
- * Logical position p of sequence b lives in row
- *   block_table[b * max_blocks_per_seq + p / block_size] * block_size + p % block_size. */
+/* Paged latent cache.  Each token's row is [c_KV || k_R], d_c + d_rope values
+ * ([ZQ "What MLA caches..."]: the latent is the only content written to the
+ * cache; [SC]: plus the small positional component).  Logical position p of
+ * sequence b lives in physical block
+ *   k = block_table[b * max_blocks_per_seq + p / block_size]
+ * at offset o = p % block_size, and each block is stored transposed:
+ *   pool: [num_blocks][d_c + d_rope][block_size] of dtype, element e of that
+ *   token at pool[(k * (d_c + d_rope) + e) * block_size + o].
+ * (Element-major blocks let the decode kernel fetch whole contiguous runs of a
+ * block per copy and feed them to the tensor cores as either operand layout.) */
 typedef struct {
   void* pool;                   /* device */
   int num_blocks;

@@ -31,7 +31,8 @@ class DeviceLayer:
         self.dt = tdtype(w.dtype)
         self.cfg = M.make_config(d, w.dtype)
         self.W = {k: to_dev(v, w.dtype, device) for k, v in p.weights.items()}
-        self.pool = torch.full((p.num_blocks, d.block_size, d.row), float("nan"), dtype=self.dt, device=device)
+        # each block stored transposed: [row element][block_size tokens]; NaN sentinels everywhere unwritten
+        self.pool = torch.full((p.num_blocks, d.row, d.block_size), float("nan"), dtype=self.dt, device=device)
         self.block_table = torch.from_numpy(p.block_table).to(device)
         if max_pos is None:
             max_pos = int(p.block_table.shape[1]) * d.block_size + 8
@@ -54,20 +55,22 @@ class DeviceLayer:
         self.ws = {}
 
     # ---------------------------------------------------------------- cache fill
-    def pool_rows(self):
-        return self.pool.view(-1, self.p.dims.row)
-
     def fill_direct(self):
         """Write drawn latent rows at every cached position (no projection involved)."""
         p, d = self.p, self.p.dims
-        flat = self.pool_rows()
+        bs = d.block_size
         for b in range(p.w.batch):
             L = int(p.lens[b])
             if L == 0:
                 continue
-            rows = I.draw_latent_rows(p.w, b, L)
-            slots = I.paged_slots(p.block_table, b, np.arange(L), d.block_size)
-            flat[torch.from_numpy(slots).to(self.device)] = to_dev(rows, p.w.dtype, self.device)
+            rows = to_dev(I.draw_latent_rows(p.w, b, L), p.w.dtype, self.device)
+            n_full = L // bs
+            if n_full:
+                blks = torch.from_numpy(p.block_table[b, :n_full].astype(np.int64)).to(self.device)
+                self.pool[blks] = rows[:n_full * bs].reshape(n_full, bs, d.row).transpose(1, 2)
+            rem = L - n_full * bs
+            if rem:
+                self.pool[int(p.block_table[b, n_full]), :, :rem] = rows[n_full * bs:].T
 
     def fill_by_append(self, chunk: int = 8192):
         """Build the cache from x_ctx with mla_compress_append (positions 0..L_b-1)."""
@@ -137,18 +140,17 @@ class DeviceLayer:
     def pool_token_bits(self) -> np.ndarray:
         """Raw bit patterns of the whole pool as [num_blocks, block_size, row] (int16 for bf16, int32 for fp32)."""
         raw = self.pool.view(torch.int16 if self.p.w.dtype == "bf16" else torch.int32)
-        return raw.cpu().numpy()
+        return raw.transpose(1, 2).cpu().numpy()
 
     def cache_rows_at(self, seq, pos) -> np.ndarray:
         """Rows at logical positions pos[i] of sequences seq[i], read back from the pool (float32 numpy)."""
         bs = self.p.dims.block_size
         seq, pos = np.asarray(seq, dtype=np.int64), np.asarray(pos, dtype=np.int64)
-        slots = self.p.block_table[seq, pos // bs].astype(np.int64) * bs + pos % bs
-        return self.pool_rows()[torch.from_numpy(slots).to(self.device)].float().cpu().numpy()
+        blk = torch.from_numpy(self.p.block_table[seq, pos // bs].astype(np.int64)).to(self.device)
+        off = torch.from_numpy(pos % bs).to(self.device)
+        return self.pool[blk, :, off].float().cpu().numpy()
 
     def cache_rows_logical(self, b: int, n: int | None = None) -> np.ndarray:
         """Rows 0..n-1 of sequence b read back from the pool, as float32 numpy (exact bf16 values)."""
-        p, d = self.p, self.p.dims
-        n = int(p.kv_len[b]) if n is None else n
-        slots = I.paged_slots(p.block_table, b, np.arange(n), d.block_size)
-        return self.pool_rows()[torch.from_numpy(slots).to(self.device)].float().cpu().numpy()
+        n = int(self.p.kv_len[b]) if n is None else n
+        return self.cache_rows_at(np.full(n, b), np.arange(n))

@@ -37,14 +37,14 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes, int device);
 
 __device__ __forceinline__ void flag_error(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
 
-// Resolved logical -> physical row of the paged cache, or -1 (and a flag) when
-// any index is out of range.
-__device__ __forceinline__ long long cache_row(const int32_t* table, int max_blocks, int num_blocks,
-                                               int block_size, int b, int pos) {
+// Physical block holding logical position `pos` of sequence b, or -1 when any index is out of range.
+// The pool stores each block transposed, [row element][block_size tokens]: element e of the token at
+// offset o of block k lives at ((k * row_width + e) * block_size + o).
+__device__ __forceinline__ int cache_block(const int32_t* table, int max_blocks, int num_blocks, int block_size,
+                                           int b, int pos) {
   if (pos < 0 || pos >= max_blocks * block_size) return -1;
-  int blk = table[(long long)b * max_blocks + pos / block_size];
-  if (blk < 0 || blk >= num_blocks) return -1;
-  return (long long)blk * block_size + pos % block_size;
+  const int blk = table[(long long)b * max_blocks + pos / block_size];
+  return (blk < 0 || blk >= num_blocks) ? -1 : blk;
 }
 
 // ------------------------------------------------------------------ launch plumbing

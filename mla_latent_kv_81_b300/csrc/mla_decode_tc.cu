@@ -7,23 +7,30 @@
 // at decode time": attention runs in the latent space after the key
 // up-projection is folded into the query).
 //
+// The pool stores every block transposed, [576 elements][64 tokens], so one TMA
+// box carries a contiguous run of element rows of a block, and the rows serve
+// as either MMA operand layout: tokens-contiguous (MN-major) B for the scores,
+// K-major B for the values.
+//
 // A full fp32 accumulator O (128 heads x 512) fills all of one SM's tensor
 // memory, so each unit of work runs on a cluster of two CTAs:
-//   * the score CTA (rank 0) keeps the latent part of the absorbed query in
-//     TMEM and its positional part in shared memory, streams the cache in
-//     128-token tiles (two blocks) through a ring of 16 KB chunk slots with
-//     TMA, computes S = Q K^T with N = 128 MMAs (the tensor core runs N = 64
-//     at about 60% of its rate), and runs the online softmax with two threads
-//     per head row (one per 64-token half); each half is one unit of bf16 P,
-//     staged with its per-row rescale factor in shared memory and shipped to
-//     the value CTA's shared memory by one bulk copy;
-//   * the value CTA (rank 1) streams the [64 x 512] latent part of every block
-//     as two 32 KB halves and accumulates O += P V in all 512 TMEM columns;
-//     two warpgroups rescale O when the running maximum jumps (rarely) and
-//     write the result.
-// The cached tokens of all queries are cut into equal ranges of 128-token
-// tiles, one per cluster (split-KV); ranges that cover part of a query write
-// fp32 partials that a second kernel merges by log-sum-exp.
+//   * the score CTA (rank 0) streams the cache in 128-token tiles (two blocks,
+//     joined through the B descriptor's leading byte offset) through a ring of
+//     24 KB slots and computes S = Q K^T with N = 128 MMAs issued from
+//     compile-time operand offsets; the absorbed query of each piece arrives by
+//     TMA through the same ring and is copied into tensor memory with
+//     tcgen05.cp behind the previous piece's MMAs (its positional part goes to
+//     shared memory, gated by a free/full barrier pair); two threads per head
+//     row run the online softmax, and each 64-token unit of bf16 P is staged
+//     with its rescale factor and shipped to the value CTA by one bulk copy;
+//   * the value CTA (rank 1) streams the 512 latent rows of every block as two
+//     32 KB boxes and accumulates O += P V in all 512 TMEM columns; two
+//     warpgroups rescale O when the running maximum jumps (rarely) and write
+//     the result.
+// Every cluster plans its own work in its prologue: the visible 128-token tiles
+// of all queries are cut into equal contiguous ranges, one per cluster
+// (split-KV); ranges that cover part of a query write fp32 partials that a
+// second kernel, launched as a programmatic dependent, merges by log-sum-exp.
 #include <math.h>
 
 #include <mutex>
@@ -38,11 +45,15 @@ using namespace sm100;
 constexpr int kH = 128, kDC = 512, kDR = 64, kRow = 576, kBlk = 64;
 constexpr int kTile = 2 * kBlk;                     // tokens per score tile: N of the score MMAs
 constexpr int kThreads = 384;                       // warps 0-3: TMA, MMA, TMEM, spare; 4-11: two warpgroups
-constexpr int kBoxBytes = 64 * 64 * 2;              // one swizzled [64 tokens x 64 elements] box
-constexpr int kChunks = kRow / 64;                  // 9 chunks per cached row: 8 latent + 1 positional
-constexpr int kSlotK = 2 * kBoxBytes;               // score ring slot: one chunk of a 128-token tile
-constexpr int kRing = 10;
-constexpr int kSlotV = 4 * kBoxBytes;               // value ring slot: four latent chunks of one block
+// The pool stores each block transposed, [576 elements][64 tokens] (128 B per element row), so a TMA box
+// of whole element rows is one contiguous run of the block.
+constexpr int kE = 96;                              // elements per score-ring box: 6 boxes cover a block
+constexpr int kSlotsPerTile = kRow / kE;            // ring slots per 128-token tile
+constexpr int kBoxK = kE * 128;                     // one block's kE element rows (12 KB)
+constexpr int kSlotK = 2 * kBoxK;                   // score ring slot: the same rows of the tile's two blocks
+constexpr int kRing = 7;
+constexpr int kVRows = 256;                         // latent rows per value box: the N of one P.V MMA group
+constexpr int kSlotV = kVRows * 128;                // value ring slot (32 KB)
 constexpr int kVRing = 5;
 constexpr int kPSlots = 3;                          // P units (64 tokens) in flight to the value CTA
 constexpr int kSlotBytes = 18432;                   // P 16 KB | alpha | l (tokens 0-63) | l (64-127) | m
@@ -56,7 +67,9 @@ constexpr int kOffStage = kOffRing + kRing * kSlotK;  // score CTA: each warpgro
 constexpr int kSmemScore = kOffStage + 2 * kSlotBytes;
 constexpr int kSmemValue = kOffSlots + kPSlots * kSlotBytes;
 constexpr int kSmemBytes = (kSmemScore > kSmemValue ? kSmemScore : kSmemValue) + 1024;  // + alignment slack
-static_assert(kOffRing % 1024 == 0 && kOffSlots % 1024 == 0 && kOffStage % 1024 == 0 && kSlotBytes % 1024 == 0,
+static_assert(kRow % kE == 0 && kE % 16 == 0 && kDC % 16 == 0, "score slots hold whole K-steps");
+static_assert(kOffRing % 1024 == 0 && kOffSlots % 1024 == 0 && kOffStage % 1024 == 0 && kSlotBytes % 1024 == 0 &&
+                  kBoxK % 1024 == 0 && kSlotV % 1024 == 0,
               "swizzle alignment");
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTxUnit = 16384 + 512;
@@ -65,19 +78,24 @@ constexpr uint32_t kTxLast = kTxUnit + 1536;
 constexpr int kSCol = 0, kQCol = 256;
 constexpr float kRescaleThreshold = 8.0f;            // log2 units: rescale O only when the max grows by 2^8
 
-enum : int { kCmdRescale = 1, kCmdEpilogue = 2, kCmdExit = 3 };
+constexpr int kQChunks = kDC / 64;                  // latent query chunks of 64 columns per piece
+constexpr uint32_t kQChunkBytes = kH * 128;          // one chunk: [128 heads][64 bf16] (16 KB)
+static_assert(kQChunkBytes <= (uint32_t)kSlotK, "a query chunk travels in one score-ring slot");
 
+enum : int { kCmdRescale = 1, kCmdEpilogue = 2, kCmdZero = 3, kCmdExit = 4 };
+
+// A contiguous range of one query's visible tokens processed by one cluster.
 struct Piece {
   int item;     // b * n_q + j
   int t_begin;  // first token (multiple of 128)
-  int t_end;    // one past the last token
+  int t_end;    // one past the last token (== t_begin: the query sees nothing)
   int slot;     // partial slot, or -1 when the piece is the whole query
 };
 
 struct Ctrl {
   uint64_t k_full[kRing], k_empty[kRing];
   uint64_t s_full[2], s_empty[2];
-  uint64_t q_ready;
+  uint64_t qr_full, qr_free;               // positional query part in shared memory: loaded / free again
   uint64_t stage_free[2], stage_full[2];   // per warpgroup: its P staging buffer may be written / is written
   uint64_t xch[2];
   uint64_t p_empty[kPSlots];
@@ -86,7 +104,10 @@ struct Ctrl {
   uint64_t mma_idle, work, done;
   uint32_t tmem_base;
   int abort_flag;
-  int cmd, cmd_slot, cmd_piece;
+  int cmd, cmd_slot;
+  Piece cmd_piece;
+  // this cluster's share of the tiles, [lo, hi), and where its scan of the queries starts
+  int plan_lo, plan_hi, plan_item, plan_prefix, plan_total, plan_last;
   float l_buf[kH];
   float m_buf[kH];
   float half_max[2][2][kH];   // [tile parity][token half][row]
@@ -96,10 +117,10 @@ static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
 struct Params {
   const bf16* q;
   const int32_t* table;
+  const int32_t* kv_len;
   int max_blocks, num_blocks;
-  int n_q;
-  const Piece* pieces;
-  const int2* cluster_range;
+  int n_q, items, cap;        // cap = max_blocks * block size
+  int* prefix;                // [items + 1]: exclusive prefix of visible tiles (written by CTA 0)
   bf16* o_lat;
   float* lse_out;
   float* part_o;
@@ -117,43 +138,6 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Walks a cluster's pieces in steps of `step` tokens.
-struct TileCursor {
-  int pi, end, t, t_end, b, step;
-  __device__ void start(const Piece* pieces, int first, int last, int n_q, int step_) {
-    pi = first - 1;
-    end = last;
-    t = t_end = 0;
-    b = 0;
-    step = step_;
-    next_piece(pieces, n_q);
-  }
-  __device__ void next_piece(const Piece* pieces, int n_q) {
-    while (++pi < end) {
-      const Piece pc = pieces[pi];
-      if (pc.t_end > pc.t_begin) {
-        t = pc.t_begin;
-        t_end = pc.t_end;
-        b = pc.item / n_q;
-        return;
-      }
-    }
-  }
-  __device__ bool valid() const { return pi < end; }
-  __device__ void advance(const Piece* pieces, int n_q) {
-    t += step;
-    if (t >= t_end) next_piece(pieces, n_q);
-  }
-};
-
-// Block-table entries are loaded this many steps before their TMA loads and checked only when used,
-// so the latency of the table read never sits in front of a load.
-constexpr int kLookahead = 4;
-
-// Table entry `idx` of sequence b, loaded but not yet checked.
-__device__ __forceinline__ int table_raw(const Params& p, int b, int idx) {
-  return __ldg(p.table + (long long)b * p.max_blocks + idx);
-}
 // A loaded entry as a physical block (0 and a flag when it is out of range).
 __device__ __forceinline__ int checked_block(const Params& p, int blk, bool flag) {
   if (blk < 0 || blk >= p.num_blocks) {
@@ -177,47 +161,21 @@ __device__ __forceinline__ bool warp_wait_cta(uint64_t* bar, uint32_t parity, ui
   return __all_sync(0xffffffffu, ok);
 }
 
-// ------------------------------------------------------------------ planner
-// One CTA of 1024 threads.  Cuts the visible 128-token tiles of all queries into C
-// equal contiguous ranges (cluster c gets global tiles [c*T/C, (c+1)*T/C))
-// and lists the resulting pieces in global tile order.
-constexpr int kPlanThreads = 1024;
+// ------------------------------------------------------------------ work plan
+// The visible 128-token tiles of all queries, in query order, are cut into C equal contiguous ranges,
+// one per cluster: cluster c takes global tiles [c T / C, (c + 1) T / C) (C = min(clusters, T)).  A
+// query with nothing visible belongs to the cluster whose range holds its position in that order (the
+// last cluster when it sits at the end).  A piece that covers part of a query writes a partial into
+// slot 2c when it continues a query begun by an earlier cluster, else into slot 2c + 1.
 
-__device__ int block_scan_excl(int v, int* sh, int& total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+__device__ __forceinline__ int visible_tokens(const Params& p, int item, bool flag) {
+  const int b = item / p.n_q, j = item - b * p.n_q;
+  int kv = __ldg(p.kv_len + b);
+  if (kv < 0 || kv > p.cap) {
+    if (flag) flag_error(p.status, kFlagIndex);
+    kv = kv < 0 ? 0 : p.cap;
   }
-  if (lane == 31) sh[wid] = x;
-  __syncthreads();
-  if (wid == 0) {
-    int w = sh[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    sh[lane] = w;
-  }
-  __syncthreads();
-  const int excl = x - v + (wid > 0 ? sh[wid - 1] : 0);
-  total = sh[31];
-  __syncthreads();
-  return excl;
-}
-
-__device__ __forceinline__ int visible_tokens(const int32_t* kv_len, int item, int n_q, int cap, uint32_t* status,
-                                              bool flag) {
-  const int b = item / n_q, j = item % n_q;
-  int kv = kv_len[b];
-  if (kv < 0 || kv > cap) {
-    if (flag) flag_error(status, kFlagIndex);
-    kv = kv < 0 ? 0 : cap;
-  }
-  const int vis = kv - (n_q - 1 - j);
+  const int vis = kv - (p.n_q - 1 - j);
   return vis > 0 ? vis : 0;
 }
 
@@ -225,74 +183,154 @@ __device__ __forceinline__ int cluster_of(long long x, long long T, int C) {
   return (int)(((x + 1) * C + T - 1) / T) - 1;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* kv_len, int items, int n_q, int cap, int C,
-                                                            int* prefix, int2* item_range, int* slot_off,
-                                                            int2* cluster_range, Piece* pieces, uint32_t* status) {
-  __shared__ int sh[32];
-  // pass 1: exclusive prefix of visible tiles
+// Inclusive prefix sum across the warp.
+__device__ __forceinline__ int warp_scan_incl(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+// One warp of every CTA: the cluster's tile range and the first query it deals with.  CTA 0 also
+// publishes the tile prefix for the merge kernel.
+__device__ void plan_cluster(const Params& p, Ctrl* ctrl, int cid, int clusters) {
+  const int lane = threadIdx.x & 31;
+  const bool writer = blockIdx.x == 0;
   int carry = 0;
-  for (int base = 0; base < items; base += kPlanThreads) {
-    const int i = base + threadIdx.x;
-    const int tiles = i < items ? ceil_div(visible_tokens(kv_len, i, n_q, cap, status, true), kTile) : 0;
-    int tot;
-    const int ex = block_scan_excl(tiles, sh, tot);
-    if (i < items) prefix[i] = carry + ex;
-    carry += tot;
+  for (int base = 0; base < p.items; base += 32) {
+    const int i = base + lane;
+    const int tiles = i < p.items ? ceil_div(visible_tokens(p, i, writer), kTile) : 0;
+    const int x = warp_scan_incl(tiles);
+    if (writer && i < p.items) p.prefix[i] = carry + x - tiles;
+    carry += __shfl_sync(0xffffffffu, x, 31);
   }
-  const long long T = carry;
-  if (threadIdx.x == 0) prefix[items] = carry;
-  for (int c = threadIdx.x; c < C; c += kPlanThreads) cluster_range[c] = make_int2(0, 0);
-  // with fewer tiles than clusters, use one cluster per tile so that no cluster's range is empty
-  if (T < C) C = (int)T;
-  __syncthreads();
-  // pass 2: pieces per query and partial slots
-  int carry_p = 0, carry_s = 0;
-  for (int base = 0; base < items; base += kPlanThreads) {
-    const int i = base + threadIdx.x;
-    int np = 0;
-    if (i < items) {
-      const int P0 = prefix[i], P1 = prefix[i + 1];
-      if (P1 > P0) np = cluster_of(P1 - 1, T, C) - cluster_of(P0, T, C) + 1;
+  const int T = carry;
+  if (writer && lane == 0) p.prefix[p.items] = T;
+  const int Ce = max(1, min(clusters, T));
+  int lo = T + 1, hi = T + 1, item = p.items, prefix = T;
+  if (cid < Ce) {
+    lo = (int)((long long)cid * T / Ce);
+    hi = (int)((long long)(cid + 1) * T / Ce);
+    int run = 0;
+    for (int base = 0; base < p.items; base += 32) {
+      const int i = base + lane;
+      const int tiles = i < p.items ? ceil_div(visible_tokens(p, i, false), kTile) : 0;
+      const int x = warp_scan_incl(tiles);
+      const int P = run + x - tiles;
+      const bool mine = i < p.items && (tiles > 0 ? P + tiles > lo : P >= lo);
+      const uint32_t m = __ballot_sync(0xffffffffu, mine);
+      if (m) {
+        const int l0 = __ffs(m) - 1;
+        item = base + l0;
+        prefix = __shfl_sync(0xffffffffu, P, l0);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, x, 31);
     }
-    int tp, ts;
-    const int ex_p = block_scan_excl(np, sh, tp);
-    const int ex_s = block_scan_excl(np > 1 ? np : 0, sh, ts);
-    if (i < items) {
-      item_range[i] = make_int2(carry_p + ex_p, np);
-      slot_off[i] = carry_s + ex_s;
-    }
-    carry_p += tp;
-    carry_s += ts;
   }
-  __syncthreads();
-  // pass 3: write the pieces and each cluster's [first, end) range
-  for (int i = threadIdx.x; i < items; i += kPlanThreads) {
-    const int2 r = item_range[i];
-    if (r.y == 0) continue;
-    const long long P0 = prefix[i], P1 = prefix[i + 1];
-    const int vis = visible_tokens(kv_len, i, n_q, cap, status, false);
-    const int c0 = cluster_of(P0, T, C);
-    for (int k = 0; k < r.y; ++k) {
-      const int c = c0 + k;
-      const long long lo = (long long)c * T / C, hi = (long long)(c + 1) * T / C;
-      const long long a = lo > P0 ? lo : P0, e = hi < P1 ? hi : P1;
-      Piece pc;
+  if (lane == 0) {
+    ctrl->plan_lo = lo;
+    ctrl->plan_hi = hi;
+    ctrl->plan_item = item;
+    ctrl->plan_prefix = prefix;
+    ctrl->plan_total = T;
+    ctrl->plan_last = cid == Ce - 1;
+  }
+}
+
+// Walks the pieces of this cluster in order; each role of the kernel runs its own copy.
+struct PieceIter {
+  int item, prefix, lo, hi, T, cid;
+  bool last;
+  __device__ void init(const Ctrl* c, int cid_) {
+    item = c->plan_item;
+    prefix = c->plan_prefix;
+    lo = c->plan_lo;
+    hi = c->plan_hi;
+    T = c->plan_total;
+    last = c->plan_last != 0;
+    cid = cid_;
+  }
+  // The next piece, including queries with nothing visible (t_end == t_begin).
+  __device__ bool next(const Params& p, Piece& pc) {
+    while (item < p.items) {
+      const int vis = visible_tokens(p, item, false);
+      const int tiles = ceil_div(vis, kTile);
+      const int P = prefix;
+      if (P >= hi && !(last && P == T)) return false;
+      const int i = item;
+      ++item;
+      prefix += tiles;
+      if (tiles == 0) {
+        if (P >= lo) {
+          pc.item = i;
+          pc.t_begin = pc.t_end = 0;
+          pc.slot = -1;
+          return true;
+        }
+        continue;
+      }
+      const int a = max(lo, P), e = min(hi, P + tiles);
+      if (e <= a) continue;
       pc.item = i;
-      pc.t_begin = (int)(a - P0) * kTile;
-      pc.t_end = (int)(e - P0) * kTile;
-      if (pc.t_end > vis) pc.t_end = vis;
-      pc.slot = r.y > 1 ? slot_off[i] + k : -1;
-      const int idx = r.x + k;
-      pieces[idx] = pc;
-      if (lo >= P0) cluster_range[c].x = idx;
-      if (hi <= P1) cluster_range[c].y = idx + 1;
+      pc.t_begin = (a - P) * kTile;
+      pc.t_end = min(vis, (e - P) * kTile);
+      pc.slot = (a > P || e < P + tiles) ? 2 * cid + (a > P ? 0 : 1) : -1;
+      return true;
     }
+    return false;
+  }
+  __device__ bool next_nonempty(const Params& p, Piece& pc) {
+    while (next(p, pc))
+      if (pc.t_end > pc.t_begin) return true;
+    return false;
+  }
+};
+
+// Copy a [128 rows x 32 B] slice of a shared-memory matrix (descriptor) into 8 TMEM columns.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// ------------------------------------------------------------------ score MMAs
+// The kE / 16 K-steps of ring slot S of a score tile, each an M = 128 (heads), N = 128 (tokens), K = 16
+// MMA into d: K-step elements e = S * kE + 16 k.  Latent elements take A from the query's TMEM columns
+// (32 columns per 64 bf16 elements, 8 per K-step), positional elements from the shared-memory rows
+// (32 B per K-step); B advances 16 element rows (2048 B) per K-step.
+template <int S>
+__device__ __forceinline__ void score_slot_mmas_t(uint32_t d, uint32_t tq, uint64_t qr0, uint64_t bd, uint32_t idesc) {
+#pragma unroll
+  for (int k = 0; k < kE / 16; ++k) {
+    const int e = S * kE + k * 16;
+    const uint32_t acc = (S > 0 || k > 0) ? 1u : 0u;
+    if (e < kDC)
+      mma_ts(d, tq + (e / 64) * 32 + ((e % 64) / 16) * 8, bd + (uint64_t)(k * 128), idesc, acc);
+    else
+      mma_ss(d, qr0 + (uint64_t)(((e - kDC) / 16) * 2), bd + (uint64_t)(k * 128), idesc, acc);
+  }
+}
+
+// Dispatch on a slot index that is a compile-time constant wherever the caller's loop is unrolled.
+__device__ __forceinline__ void score_slot_mmas(int sl, uint32_t d, uint32_t tq, uint64_t qr0, uint64_t bd,
+                                                uint32_t idesc) {
+  static_assert(kSlotsPerTile <= 6, "dispatch covers six slots");
+  switch (sl) {
+    case 0: score_slot_mmas_t<0>(d, tq, qr0, bd, idesc); break;
+    case 1: score_slot_mmas_t<(1 < kSlotsPerTile ? 1 : 0)>(d, tq, qr0, bd, idesc); break;
+    case 2: score_slot_mmas_t<(2 < kSlotsPerTile ? 2 : 0)>(d, tq, qr0, bd, idesc); break;
+    case 3: score_slot_mmas_t<(3 < kSlotsPerTile ? 3 : 0)>(d, tq, qr0, bd, idesc); break;
+    case 4: score_slot_mmas_t<(4 < kSlotsPerTile ? 4 : 0)>(d, tq, qr0, bd, idesc); break;
+    default: score_slot_mmas_t<(5 < kSlotsPerTile ? 5 : 0)>(d, tq, qr0, bd, idesc); break;
   }
 }
 
 // ------------------------------------------------------------------ attention kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap map1, const __grid_constant__ CUtensorMap map4, Params p) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap mapk, const __grid_constant__ CUtensorMap mapv,
+                     const __grid_constant__ CUtensorMap mapq, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
@@ -301,6 +339,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int cid = (int)cluster_id_x();
   volatile int* abort_flag = &ctrl->abort_flag;
 
+  // the merge kernel may be scheduled now; it waits for this grid to finish before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < kRing; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
@@ -308,7 +348,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctrl->s_empty[i], 256);
       mbar_init(&ctrl->xch[i], 256);
     }
-    mbar_init(&ctrl->q_ready, 256);
+    mbar_init(&ctrl->qr_full, 1);
+    mbar_init(&ctrl->qr_free, 1);
     for (int i = 0; i < 2; ++i) { mbar_init(&ctrl->stage_free[i], 1); mbar_init(&ctrl->stage_full[i], 128); }
     for (int i = 0; i < kPSlots; ++i) { mbar_init(&ctrl->p_empty[i], 1); mbar_init(&ctrl->p_full[i], 1); }
     for (int i = 0; i < kVRing; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
@@ -323,133 +364,119 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&map1);
-    prefetch_tmap(&map4);
+    prefetch_tmap(&mapk);
+    prefetch_tmap(&mapv);
+    prefetch_tmap(&mapq);
   }
+  if (warp == 3) plan_cluster(p, ctrl, cid, (int)num_clusters_x());
   tc_fence_before();
   __syncthreads();
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
-  const int2 range = p.cluster_range[cid];
   const uint32_t smem_base = smem_u32(smem);
   // warpgroup lanes: warps 4..11, quarter q4 = TMEM lane group, half = which 64 tokens / 256 O columns
   const int q4 = warp & 3, half = (warp - 4) >> 2;
   const int h = q4 * 32 + lane;
+  PieceIter it;
+  it.init(ctrl, cid);
+  Piece pc;
 
   if (rank == 0) {
     // =========================== score CTA ===========================
     if (warp == 0) {
       if (lane == 0) {
-        // ring slot = one 64-element chunk of a 128-token tile: chunk c of the tile's first block at +0,
-        // of its second block at +8 KB (absent in a one-block tail tile)
-        int r = 0;
+        // per piece: the 8 latent query chunks (16 KB each, through the ring), the positional query chunk
+        // (into QR once the previous piece's MMAs are done with it), then the tiles.  A tile slot holds
+        // element rows [sl * kE, sl * kE + kE) of the tile's first block at +0 and of its second block at
+        // +kBoxK (absent in a one-block tail tile).  Block-table entries are read one tile ahead.
+        int r = 0, npiece = 0;
         uint32_t phase = 0;
-        TileCursor ahead;
-        ahead.start(p.pieces, range.x, range.y, p.n_q, kTile);
-        // raw entries of the next kLookahead tiles; bit u of `live` / `two`: tile u exists / has a second block
-        int raw0[kLookahead], raw1[kLookahead];
-        uint32_t live = 0, two = 0;
-#pragma unroll
-        for (int u = 0; u < kLookahead; ++u) {
-          raw0[u] = raw1[u] = 0;
-          if (ahead.valid()) {
-            live |= 1u << u;
-            raw0[u] = table_raw(p, ahead.b, ahead.t / kBlk);
-            if (ahead.t + kBlk < ahead.t_end) { two |= 1u << u; raw1[u] = table_raw(p, ahead.b, ahead.t / kBlk + 1); }
-            ahead.advance(p.pieces, p.n_q);
+        while (it.next_nonempty(p, pc)) {
+          const int32_t* trow = p.table + (long long)(pc.item / p.n_q) * p.max_blocks;
+          int raw0 = __ldg(trow + pc.t_begin / kBlk);
+          int raw1 = pc.t_begin + kBlk < pc.t_end ? __ldg(trow + pc.t_begin / kBlk + 1) : 0;
+#pragma unroll 1
+          for (int c = 0; c < kQChunks; ++c) {
+            if (!mbar_wait_cta(&ctrl->k_empty[r], phase ^ 1, p.status, abort_flag)) goto score_done;
+            mbar_arrive_expect_tx(&ctrl->k_full[r], kQChunkBytes);
+            tma_load_3d(smem + kOffRing + r * kSlotK, &mapq, &ctrl->k_full[r], c * 64, 0, pc.item);
+            if (++r == kRing) { r = 0; phase ^= 1; }
           }
-        }
-        while (live & 1u) {
-#pragma unroll
-          for (int u = 0; u < kLookahead; ++u) {
-            if (!(live & (1u << u))) break;
-            const int b0 = checked_block(p, raw0[u], true);
-            const int b1 = (two & (1u << u)) ? checked_block(p, raw1[u], true) : -1;
-            live &= ~(1u << u);
-            two &= ~(1u << u);
-            if (ahead.valid()) {   // refill this entry with the tile kLookahead steps ahead
-              live |= 1u << u;
-              raw0[u] = table_raw(p, ahead.b, ahead.t / kBlk);
-              if (ahead.t + kBlk < ahead.t_end) { two |= 1u << u; raw1[u] = table_raw(p, ahead.b, ahead.t / kBlk + 1); }
-              ahead.advance(p.pieces, p.n_q);
+          if (!mbar_wait_cta(&ctrl->qr_free, (npiece & 1) ^ 1, p.status, abort_flag)) goto score_done;
+          mbar_arrive_expect_tx(&ctrl->qr_full, kQChunkBytes);
+          tma_load_3d(smem + kOffQR, &mapq, &ctrl->qr_full, kDC, 0, pc.item);
+          for (int t = pc.t_begin; t < pc.t_end; t += kTile) {
+            const bool two = t + kBlk < pc.t_end;
+            const int b0 = checked_block(p, raw0, true);
+            const int b1 = two ? checked_block(p, raw1, true) : -1;
+            const int tn = t + kTile;
+            if (tn < pc.t_end) {
+              raw0 = __ldg(trow + tn / kBlk);
+              if (tn + kBlk < pc.t_end) raw1 = __ldg(trow + tn / kBlk + 1);
             }
 #pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
+            for (int sl = 0; sl < kSlotsPerTile; ++sl) {
               if (!mbar_wait_cta(&ctrl->k_empty[r], phase ^ 1, p.status, abort_flag)) goto score_done;
               uint8_t* dst = smem + kOffRing + r * kSlotK;
-              mbar_arrive_expect_tx(&ctrl->k_full[r], b1 >= 0 ? 2 * kBoxBytes : kBoxBytes);
-              tma_load_4d(dst, &map1, &ctrl->k_full[r], 0, 0, c, b0);
-              if (b1 >= 0) tma_load_4d(dst + kBoxBytes, &map1, &ctrl->k_full[r], 0, 0, c, b1);
+              mbar_arrive_expect_tx(&ctrl->k_full[r], two ? kSlotK : kBoxK);
+              tma_load_3d(dst, &mapk, &ctrl->k_full[r], 0, sl * kE, b0);
+              if (two) tma_load_3d(dst + kBoxK, &mapk, &ctrl->k_full[r], 0, sl * kE, b1);
               if (++r == kRing) { r = 0; phase ^= 1; }
             }
           }
+          ++npiece;
         }
       }
     } else if (warp == 1) {
       if (lane == 0) {
-        // S[128 heads x 128 tokens] = Q K^T over 9 chunks of 4 K-steps; latent chunks take A from TMEM,
-        // the positional chunk from shared memory; every chunk's slot is released when its MMAs complete
-        const uint32_t idesc = idesc_bf16(128, kTile, false, false);
-        const uint64_t ring0 = desc_sw128(smem_base + kOffRing, 16, 1024);
+        // S[128 heads x 128 tokens] = Q K^T: the cached rows are the MN-major B operand (tokens contiguous),
+        // the tile's two blocks one box apart (leading byte offset kBoxK), 8-element groups 1024 B apart;
+        // latent K-steps take A from TMEM, positional K-steps from shared memory
+        const uint32_t idesc = idesc_bf16(128, kTile, false, true);
+        const uint64_t ring0 = desc_sw128(smem_base + kOffRing, kBoxK, 1024);
         const uint64_t qr0 = desc_sw128(smem_base + kOffQR, 16, 1024);
-        int r = 0, sbuf = 0;
-        uint32_t kphase = 0, sphase = 0, qphase = 0;
-        for (int pi = range.x; pi < range.y; ++pi) {
-          const Piece pc = p.pieces[pi];
-          if (pc.t_end <= pc.t_begin) continue;
-          if (!mbar_wait(&ctrl->q_ready, qphase, p.status, abort_flag)) goto score_done;
-          qphase ^= 1;
+        const uint64_t qchunk0 = desc_sw128(smem_base + kOffRing, 16, 1024);
+        const uint32_t tq = tmem + kQCol;
+        int r = 0, sbuf = 0, npiece = 0;
+        uint32_t kphase = 0, sphase = 0;
+        while (it.next_nonempty(p, pc)) {
+          // the piece's latent query into TMEM: tcgen05 operations of this thread run in issue order, so
+          // the copies land only after the previous piece's MMAs have read the old query
+#pragma unroll 1
+          for (int c = 0; c < kQChunks; ++c) {
+            if (!mbar_wait_cta(&ctrl->k_full[r], kphase, p.status, abort_flag)) goto score_done;
+            tc_fence_after();
+            const uint64_t sd = qchunk0 + (uint64_t)(r * (kSlotK >> 4));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) tmem_cp_128x256b(tq + c * 32 + k * 8, sd + (uint64_t)(k * 2));
+            mma_commit(&ctrl->k_empty[r]);
+            if (++r == kRing) { r = 0; kphase ^= 1; }
+          }
           for (int t = pc.t_begin; t < pc.t_end; t += kTile) {
             if (!mbar_wait_cta(&ctrl->s_empty[sbuf], sphase ^ 1, p.status, abort_flag)) goto score_done;
+            tc_fence_after();
             const uint32_t d = tmem + kSCol + sbuf * kTile;
-            // the tile's 9 chunks are accumulated in the order they land (their loads complete out of
-            // order), so a late chunk does not hold the slots of the chunks behind it
-            uint32_t pending = (1u << kChunks) - 1;
-            uint32_t acc = 0;
-            const long long t0 = clock64();
-            while (pending) {
-              bool progress = false;
 #pragma unroll
-              for (int c = 0; c < kChunks; ++c) {
-                if (!(pending & (1u << c))) continue;
-                int rc = r + c;
-                uint32_t ph = kphase;
-                if (rc >= kRing) { rc -= kRing; ph ^= 1; }
-                if (!mbar_poll_cta(smem_u32(&ctrl->k_full[rc]), ph)) continue;
-                tc_fence_after();
-                const uint64_t kd = ring0 + (uint64_t)(rc * (kSlotK >> 4));
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  if (c < kChunks - 1)
-                    mma_ts(d, tmem + kQCol + c * 32 + k * 8, kd + (uint64_t)(k * 2), idesc, (acc | k) ? 1u : 0u);
-                  else
-                    mma_ss(d, qr0 + (uint64_t)(k * 2), kd + (uint64_t)(k * 2), idesc, (acc | k) ? 1u : 0u);
-                }
-                acc = 1;
-                mma_commit(&ctrl->k_empty[rc]);
-                pending &= ~(1u << c);
-                progress = true;
+            for (int sl = 0; sl < kSlotsPerTile; ++sl) {
+              if (!mbar_wait_cta(&ctrl->k_full[r], kphase, p.status, abort_flag)) goto score_done;
+              if (sl == kSlotsPerTile - 1 && t == pc.t_begin) {
+                // the positional query part of this piece (read by the last slot's K-steps)
+                if (!mbar_wait_cta(&ctrl->qr_full, npiece & 1, p.status, abort_flag)) goto score_done;
               }
-              if (!progress) {
-                // nothing landed: doze on the oldest outstanding chunk for a moment
-                int rc = r + __ffs(pending) - 1;
-                uint32_t ph = kphase;
-                if (rc >= kRing) { rc -= kRing; ph ^= 1; }
-                mbar_test_sleep(smem_u32(&ctrl->k_full[rc]), ph, 200u);
-                if (*abort_flag) goto score_done;
-                if (clock64() - t0 > kTimeoutCycles) {
-                  atomicOr(p.status, kFlagTimeout);
-                  *abort_flag = 1;
-                  goto score_done;
-                }
-              }
+              tc_fence_after();
+              // every MMA operand of the slot is a compile-time offset from two base registers: any runtime
+              // arithmetic between the MMAs of a slot stalls their issue
+              score_slot_mmas(sl, d, tq, qr0, ring0 + (uint64_t)(r * (kSlotK >> 4)), idesc);
+              mma_commit(&ctrl->k_empty[r]);
+              if (++r == kRing) { r = 0; kphase ^= 1; }
             }
-            r += kChunks;
-            if (r >= kRing) { r -= kRing; kphase ^= 1; }
             mma_commit(&ctrl->s_full[sbuf]);
             if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
           }
+          // QR (and the TMEM query) may be replaced once this piece's MMAs complete
+          mma_commit(&ctrl->qr_free);
+          ++npiece;
         }
       }
     } else if (warp >= 4 && warp < 12) {
@@ -458,33 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t peer_slots = mapa(smem_base + kOffSlots, 1);
       int sbuf = 0, tile = 0, unit = 0;
       uint32_t sphase = 0, stage_phase = 0;
-      for (int pi = range.x; pi < range.y; ++pi) {
-        const Piece pc = p.pieces[pi];
-        if (pc.t_end <= pc.t_begin) continue;
-        {
-          // absorbed query row h: latent chunks 4*half .. 4*half+3 -> TMEM; the positional part -> the
-          // swizzled shared-memory rows the MMA reads as A
-          const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)pc.item * kH + h) * kRow);
-#pragma unroll 1
-          for (int c = 4 * half; c < 4 * half + 4; ++c) {
-            uint32_t r[32];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint4 v = __ldg(src + c * 8 + i);
-              r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
-            }
-            tmem_st32(lane_base + kQCol + c * 32, r);
-          }
-          if (half == 1) {
-            uint8_t* qr = smem + kOffQR + h * 128;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(qr + ((u ^ (h & 7)) << 4)) = __ldg(src + 64 + u);
-            fence_proxy_async_smem();
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&ctrl->q_ready);
-        }
+      while (it.next_nonempty(p, pc)) {
         float m = -INFINITY, lpart = 0.f;
         for (int t = pc.t_begin; t < pc.t_end; t += kTile, ++tile) {
           const int ntok = min(kTile, pc.t_end - t);
@@ -598,54 +599,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // =========================== value CTA ===========================
     if (warp == 0) {
       if (lane == 0) {
-        // ring slot = latent chunks 0-3 or 4-7 of one 64-token block
+        // ring slot = latent element rows [0, 256) or [256, 512) of one 64-token block; block-table entries
+        // are read one block ahead
         int r = 0;
         uint32_t phase = 0;
-        TileCursor ahead;
-        ahead.start(p.pieces, range.x, range.y, p.n_q, kBlk);
-        constexpr int kLA = 2 * kLookahead;   // blocks ahead
-        int raw[kLA];
-        uint32_t live = 0;
-#pragma unroll
-        for (int u = 0; u < kLA; ++u) {
-          raw[u] = 0;
-          if (ahead.valid()) {
-            live |= 1u << u;
-            raw[u] = table_raw(p, ahead.b, ahead.t / kBlk);
-            ahead.advance(p.pieces, p.n_q);
-          }
-        }
-        while (live & 1u) {
-#pragma unroll
-          for (int u = 0; u < kLA; ++u) {
-            if (!(live & (1u << u))) break;
-            const int blk = checked_block(p, raw[u], false);
-            live &= ~(1u << u);
-            if (ahead.valid()) {
-              live |= 1u << u;
-              raw[u] = table_raw(p, ahead.b, ahead.t / kBlk);
-              ahead.advance(p.pieces, p.n_q);
-            }
+        while (it.next_nonempty(p, pc)) {
+          const int32_t* trow = p.table + (long long)(pc.item / p.n_q) * p.max_blocks;
+          int raw = __ldg(trow + pc.t_begin / kBlk);
+          for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
+            const int blk = checked_block(p, raw, false);
+            if (t + kBlk < pc.t_end) raw = __ldg(trow + (t + kBlk) / kBlk);
 #pragma unroll 1
             for (int nh = 0; nh < 2; ++nh) {
               if (!mbar_wait_cta(&ctrl->v_empty[r], phase ^ 1, p.status, abort_flag)) goto value_done;
               mbar_arrive_expect_tx(&ctrl->v_full[r], kSlotV);
-              tma_load_4d(smem + kOffV + r * kSlotV, &map4, &ctrl->v_full[r], 0, 0, 4 * nh, blk);
+              tma_load_3d(smem + kOffV + r * kSlotV, &mapv, &ctrl->v_full[r], 0, kVRows * nh, blk);
               if (++r == kVRing) { r = 0; phase ^= 1; }
             }
           }
         }
       }
     } else if (warp == 1) {
-      // MMA warp: lane 0 issues, the whole warp waits and zeroes tail rows
-      const uint32_t idesc = idesc_bf16(128, 256, false, true);
+      // MMA warp: lane 0 issues, the whole warp waits and zeroes tail tokens.  O[:, 256 nh .. +256] +=
+      // P (A: [heads][64 tokens], K-major) . V (B: the slot's 256 latent rows of 64 tokens, K-major)
+      const uint32_t idesc = idesc_bf16(128, kVRows, false, false);
       const uint64_t pdesc0 = desc_sw128(smem_base + kOffSlots, 16, 1024);
-      const uint64_t vdesc0 = desc_sw128(smem_base + kOffV, kBoxBytes, 1024);
+      const uint64_t vdesc0 = desc_sw128(smem_base + kOffV, 16, 1024);
       int r = 0, pslot = 0;
       uint32_t vphase = 0, pphase = 0, idle_phase = 0, done_phase = 0;
-      for (int pi = range.x; pi < range.y; ++pi) {
-        const Piece pc = p.pieces[pi];
-        if (pc.t_end <= pc.t_begin) continue;
+      while (it.next(p, pc)) {
+        if (pc.t_end <= pc.t_begin) {
+          // a query with nothing visible: the epilogue writes its zero output
+          if (lane == 0) {
+            ctrl->cmd = kCmdZero;
+            ctrl->cmd_piece = pc;
+            mbar_arrive(&ctrl->work);
+          }
+          if (!warp_wait_cta(&ctrl->done, done_phase, p.status, abort_flag)) goto value_mma_exit;
+          done_phase ^= 1;
+          continue;
+        }
         for (int t = pc.t_begin; t < pc.t_end; t += kBlk) {
           const int valid = min(kBlk, pc.t_end - t);
           const bool first = (t == pc.t_begin), last = (t + kBlk >= pc.t_end);
@@ -685,13 +678,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int nh = 0; nh < 2; ++nh) {
             if (!warp_wait_cta(&ctrl->v_full[r], vphase, p.status, abort_flag)) goto value_mma_exit;
             if (valid < kBlk) {
-              // tokens past the end of the sequence: zero their rows so 0 * garbage cannot reach O
+              // tokens past the end of the sequence: zero their columns so 0 * garbage cannot reach O.
+              // Row e holds tokens 8u..8u+7 in 16-byte unit u, stored at unit u ^ (e & 7) (128-byte swizzle)
               uint8_t* vst = smem + kOffV + r * kSlotV;
-              const int nrow = kBlk - valid;
-              for (int e = lane; e < nrow * 32; e += 32) {
-                const int box = e / (nrow * 8), rem = e % (nrow * 8);
-                const int row = valid + rem / 8, ch = rem % 8;
-                *reinterpret_cast<uint4*>(vst + box * kBoxBytes + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+              const int u_full = (valid + 7) >> 3, u_part = valid >> 3, j0 = valid & 7;
+              for (int e = lane; e < kVRows; e += 32) {
+                uint8_t* row = vst + e * 128;
+                for (int u = u_full; u < 8; ++u)
+                  *reinterpret_cast<uint4*>(row + ((u ^ (e & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+                if (j0) {
+                  uint16_t* unit = reinterpret_cast<uint16_t*>(row + ((u_part ^ (e & 7)) << 4));
+                  for (int j = j0; j < 8; ++j) unit[j] = 0;
+                }
               }
               fence_proxy_async_smem();
               __syncwarp();
@@ -701,8 +699,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint64_t pd = pdesc0 + (uint64_t)(pslot * (kSlotBytes >> 4));
               const uint64_t vd = vdesc0 + (uint64_t)(r * (kSlotV >> 4));
 #pragma unroll
-              for (int s = 0; s < 4; ++s)
-                mma_ss(tmem + nh * 256, pd + (uint64_t)(s * 2), vd + (uint64_t)(s * (2048 >> 4)), idesc,
+              for (int s = 0; s < 4; ++s)   // K-steps of 16 tokens: 32 B along both operands' rows
+                mma_ss(tmem + nh * kVRows, pd + (uint64_t)(s * 2), vd + (uint64_t)(s * 2), idesc,
                        (!first || s > 0) ? 1u : 0u);
               mma_commit(&ctrl->v_empty[r]);
             }
@@ -720,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         idle_phase ^= 1;
         if (lane == 0) {
           ctrl->cmd = kCmdEpilogue;
-          ctrl->cmd_piece = pi;
+          ctrl->cmd_piece = pc;
           mbar_arrive(&ctrl->work);
         }
         if (!warp_wait_cta(&ctrl->done, done_phase, p.status, abort_flag)) goto value_mma_exit;
@@ -757,8 +755,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tmem_st_wait();
           }
+        } else if (cmd == kCmdZero) {
+          const Piece pz = ctrl->cmd_piece;
+          uint4* dst = reinterpret_cast<uint4*>(p.o_lat + ((size_t)pz.item * kH + h) * kDC + half * 256);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          if (p.lse_out && half == 0) p.lse_out[(size_t)pz.item * kH + h] = -INFINITY;
         } else {
-          const Piece pc = p.pieces[ctrl->cmd_piece];
+          const Piece pc = ctrl->cmd_piece;
           const float l = ctrl->l_buf[h], mrow = ctrl->m_buf[h];
           const float inv = l > 0.f ? 1.f / l : 0.f;
           const float lse = l > 0.f ? (mrow + __log2f(l)) * kLn2 : -INFINITY;
@@ -818,29 +822,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ split merge
-// Block (item, g) merges columns [16 g, 16 g + 16) of all 128 heads; thread = head row.
+// Block (item, g) merges columns [16 g, 16 g + 16) of all 128 heads; thread = head row.  Launched as a
+// programmatic dependent of the attention kernel: it waits for that grid (and its writes) to complete.
+// A query's pieces lie in clusters c0..c1 (from the published tile prefix); the piece in c0 wrote
+// slot 2 c0 + 1, the one in each later cluster c slot 2 c.  Queries held by one cluster, or with
+// nothing visible, were written by the attention kernel itself.
 constexpr int kMergeGroups = kDC / 16;
 
-__global__ void __launch_bounds__(kH) merge_kernel(const Piece* pieces, const int2* item_range, const float* part_o,
+__global__ void __launch_bounds__(kH) merge_kernel(const int* prefix, int items, int clusters, const float* part_o,
                                                    const float* part_lse, bf16* o_lat, float* lse_out) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int item = blockIdx.x, g = blockIdx.y, h = threadIdx.x;
-  const int2 r = item_range[item];
-  if (r.y == 1) return;  // written directly by the attention kernel
-  uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)item * kH + h) * kDC + g * 16);
-  if (r.y == 0) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-    if (lse_out && g == 0) lse_out[(size_t)item * kH + h] = -INFINITY;
-    return;
-  }
+  const int T = prefix[items];
+  const int P0 = prefix[item], P1 = prefix[item + 1];
+  if (P1 <= P0) return;
+  const int Ce = max(1, min(clusters, T));
+  const int c0 = cluster_of(P0, T, Ce), c1 = cluster_of(P1 - 1, T, Ce);
+  if (c1 == c0) return;
   float mx = -INFINITY;
-  for (int k = 0; k < r.y; ++k) mx = fmaxf(mx, part_lse[(size_t)pieces[r.x + k].slot * kH + h]);
+  for (int c = c0; c <= c1; ++c) mx = fmaxf(mx, part_lse[(size_t)(c == c0 ? 2 * c + 1 : 2 * c) * kH + h]);
   float z = 0.f;
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  for (int k = 0; k < r.y; ++k) {
-    const int slot = pieces[r.x + k].slot;
+  for (int c = c0; c <= c1; ++c) {
+    const int slot = c == c0 ? 2 * c + 1 : 2 * c;
     const float w = expf(part_lse[(size_t)slot * kH + h] - mx);
     z += w;
     // partial layout [slot][column / 4][row][4]
@@ -855,6 +861,7 @@ __global__ void __launch_bounds__(kH) merge_kernel(const Piece* pieces, const in
     }
   }
   const float inv = 1.f / z;
+  uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)item * kH + h) * kDC + g * 16);
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     uint4 v;
@@ -918,7 +925,7 @@ int cluster_count(int device, int sm_count) {
 }
 
 struct WsLayout {
-  size_t prefix, item_range, slot_off, cluster_range, pieces, part_o, part_lse, total;
+  size_t prefix, part_o, part_lse, total;
 };
 
 WsLayout ws_layout(int items, int C) {
@@ -926,10 +933,6 @@ WsLayout ws_layout(int items, int C) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = (o + bytes + 255) / 256 * 256; return r; };
   w.prefix = take(sizeof(int) * (items + 1));
-  w.item_range = take(sizeof(int2) * items);
-  w.slot_off = take(sizeof(int) * items);
-  w.cluster_range = take(sizeof(int2) * C);
-  w.pieces = take(sizeof(Piece) * (items + C));
   w.part_o = take(sizeof(float) * (size_t)2 * C * kH * kDC);
   w.part_lse = take(sizeof(float) * (size_t)2 * C * kH);
   w.total = o;
@@ -958,61 +961,71 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   const int items = batch * n_q;
   const WsLayout w = ws_layout(items, ctx.sm_count / 2);
   char* ws = static_cast<char*>(workspace);
-  int* prefix = reinterpret_cast<int*>(ws + w.prefix);
-  int2* item_range = reinterpret_cast<int2*>(ws + w.item_range);
-  int* slot_off = reinterpret_cast<int*>(ws + w.slot_off);
-  int2* cluster_range = reinterpret_cast<int2*>(ws + w.cluster_range);
-  Piece* pieces = reinterpret_cast<Piece*>(ws + w.pieces);
 
-  // The pool viewed as [block][64-element chunk][token][element]; a box of 1 or 4 chunks lands
-  // as [chunk][token][128 B] with the 128-byte swizzle the MMA descriptors expect.
-  CUtensorMap map1, map4;
-  const cuuint64_t dims[4] = {64, (cuuint64_t)kBlk, (cuuint64_t)kChunks, (cuuint64_t)cache.num_blocks};
-  const cuuint64_t strides[3] = {(cuuint64_t)kRow * 2, 128, (cuuint64_t)kBlk * kRow * 2};
-  const cuuint32_t box1[4] = {64, (cuuint32_t)kBlk, 1, 1};
-  const cuuint32_t box4[4] = {64, (cuuint32_t)kBlk, 4, 1};
-  const cuuint32_t estride[4] = {1, 1, 1, 1};
-  if (encode(&map1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache.pool, dims, strides, box1, estride,
+  // The pool viewed as [block][element row][token] (each block stored transposed); a box of whole element
+  // rows lands as [row][64 tokens = 128 B] with the 128-byte swizzle the MMA descriptors expect.  The
+  // queries viewed as [item][head][element]; a box of 64 elements of all 128 heads lands as the K-major
+  // [head][128 B] layout of an MMA A operand.
+  CUtensorMap mapk, mapv, mapq;
+  const cuuint64_t dims[3] = {(cuuint64_t)kBlk, (cuuint64_t)kRow, (cuuint64_t)cache.num_blocks};
+  const cuuint64_t strides[2] = {(cuuint64_t)kBlk * 2, (cuuint64_t)kBlk * kRow * 2};
+  const cuuint32_t boxk[3] = {(cuuint32_t)kBlk, (cuuint32_t)kE, 1};
+  const cuuint32_t boxv[3] = {(cuuint32_t)kBlk, (cuuint32_t)kVRows, 1};
+  const cuuint64_t qdims[3] = {(cuuint64_t)kRow, (cuuint64_t)kH, (cuuint64_t)items};
+  const cuuint64_t qstrides[2] = {(cuuint64_t)kRow * 2, (cuuint64_t)kH * kRow * 2};
+  const cuuint32_t boxq[3] = {64, (cuuint32_t)kH, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  if (encode(&mapk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, cache.pool, dims, strides, boxk, estride,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-      encode(&map4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache.pool, dims, strides, box4, estride,
+      encode(&mapv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, cache.pool, dims, strides, boxv, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      encode(&mapq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qdims, qstrides, boxq, estride,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  const int cap = cache.max_blocks_per_seq * kBlk;
-  plan_kernel<<<1, kPlanThreads, 0, ctx.stream>>>(kv_len, items, n_q, cap, C, prefix, item_range, slot_off,
-                                                 cluster_range, pieces, ctx.status);
-  count_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
   Params prm;
   prm.q = static_cast<const bf16*>(q);
   prm.table = cache.block_table;
+  prm.kv_len = kv_len;
   prm.max_blocks = cache.max_blocks_per_seq;
   prm.num_blocks = cache.num_blocks;
   prm.n_q = n_q;
-  prm.pieces = pieces;
-  prm.cluster_range = cluster_range;
+  prm.items = items;
+  prm.cap = cache.max_blocks_per_seq * kBlk;
+  prm.prefix = reinterpret_cast<int*>(ws + w.prefix);
   prm.o_lat = static_cast<bf16*>(o_lat);
   prm.lse_out = lse;
   prm.part_o = reinterpret_cast<float*>(ws + w.part_o);
   prm.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
   prm.scale_log2 = scale * kLog2e;
   prm.status = ctx.status;
-  e = ensure_smem_limit((const void*)decode_tc_kernel, kSmemBytes, ctx.device);
+  cudaError_t e = ensure_smem_limit((const void*)decode_tc_kernel, kSmemBytes, ctx.device);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, ctx.stream>>>(map1, map4, prm);
+  decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, ctx.stream>>>(mapk, mapv, mapq, prm);
   count_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  merge_kernel<<<dim3(items, kMergeGroups), kH, 0, ctx.stream>>>(pieces, item_range, prm.part_o, prm.part_lse,
-                                                            prm.o_lat, lse);
+  // the merge is a programmatic dependent of the attention grid: it may be scheduled while that grid
+  // runs and waits (griddepcontrol.wait) for it to complete
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(items, kMergeGroups, 1);
+  lc.blockDim = dim3(kH, 1, 1);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = ctx.stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, merge_kernel, (const int*)prm.prefix, items, C, (const float*)prm.part_o,
+                         (const float*)prm.part_lse, prm.o_lat, lse);
   count_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace mla
-

@@ -282,34 +282,70 @@ __global__ void absorb_reduce_kernel(const float* part, int splits, int N, int H
 }
 
 // Cache rows [c || RoPE(k_R)] from the k-split partials [splits][T][d_c + d_r] of the fused
-// W_DKV / W_KR GEMM, scattered into the paged pool.  Block (t, column group of 4 * blockDim).
-__global__ void compress_reduce_kernel(const float* part, int splits, int T, int d_c, int d_r,
-                                       const int32_t* seq_idx, const int32_t* pos, const float* rope, int rope_max,
-                                       bf16* pool, int num_blocks, const int32_t* table, int max_blocks, int batch,
-                                       int block_size, uint32_t* status) {
-  const int t = blockIdx.x;
+// W_DKV / W_KR GEMM, scattered into the paged pool, which stores each block transposed
+// ([d_c + d_r][block_size]).  Block (32-token group, 64-column group): the partials are read token by
+// token (coalesced), summed, rotated and rounded, transposed through shared memory and written column
+// by column, so that tokens at consecutive positions of one block write contiguous bytes.
+constexpr int kAppTok = 32, kAppCols = 64;
+
+__global__ void __launch_bounds__(256) compress_reduce_kernel(const float* part, int splits, int T, int d_c, int d_r,
+                                                              const int32_t* seq_idx, const int32_t* pos,
+                                                              const float* rope, int rope_max, bf16* pool,
+                                                              int num_blocks, const int32_t* table, int max_blocks,
+                                                              int batch, int block_size, uint32_t* status) {
+  __shared__ bf16 tile[kAppCols][kAppTok + 2];
+  __shared__ long long dst_base[kAppTok];   // pool offset of column 0 of each token, or -1 (skipped)
+  __shared__ int tok_pos[kAppTok];
+  const int t0 = blockIdx.x * kAppTok, c0 = blockIdx.y * kAppCols;
   const int width = d_c + d_r;
-  const int col = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
-  if (col >= width) return;
-  const int b = seq_idx[t], p = pos[t];
-  long long row = -1;
-  if (b >= 0 && b < batch && p < rope_max) row = cache_row(table, max_blocks, num_blocks, block_size, b, p);
-  if (row < 0) {
-    if (col == 0) flag_error(status, kFlagIndex);
-    return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < kAppTok) {
+    const int t = t0 + threadIdx.x;
+    long long base = -1;
+    int p = 0;
+    if (t < T) {
+      const int b = seq_idx[t];
+      p = pos[t];
+      int blk = -1;
+      if (b >= 0 && b < batch && p >= 0 && p < rope_max)
+        blk = cache_block(table, max_blocks, num_blocks, block_size, b, p);
+      if (blk < 0) {
+        if (blockIdx.y == 0) flag_error(status, kFlagIndex);
+      } else {
+        base = (long long)blk * width * block_size + p % block_size;
+      }
+    }
+    dst_base[threadIdx.x] = base;
+    tok_pos[threadIdx.x] = p;
   }
-  const float4 v = sum_splits4(part, splits, (long long)T * width, (long long)t * width + col);
-  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(pool + row * width + col);
-  if (col < d_c) {
-    dst[0] = __floats2bfloat162_rn(v.x, v.y);
-    dst[1] = __floats2bfloat162_rn(v.z, v.w);
-  } else {
-    const float* cs = rope + ((long long)p * (d_r / 2) + (col - d_c) / 2) * 2;
-    float o0, o1, o2, o3;
-    rope2(v.x, v.y, cs, o0, o1);
-    rope2(v.z, v.w, cs + 2, o2, o3);
-    dst[0] = __floats2bfloat162_rn(o0, o1);
-    dst[1] = __floats2bfloat162_rn(o2, o3);
+  __syncthreads();
+  // lane l holds columns c0 + 2l and c0 + 2l + 1 of token i (a RoPE pair when in the k_R part)
+  const int col = c0 + 2 * lane;
+  for (int i = warp; i < kAppTok; i += 8) {
+    if (t0 + i >= T || col >= width || dst_base[i] < 0) continue;
+    const long long idx = (long long)(t0 + i) * width + col;
+    float2 v = *reinterpret_cast<const float2*>(part + idx);
+    for (int sp = 1; sp < splits; ++sp) {
+      const float2 w = *reinterpret_cast<const float2*>(part + (long long)sp * T * width + idx);
+      v.x += w.x;
+      v.y += w.y;
+    }
+    if (col >= d_c) {
+      const float* cs = rope + ((long long)tok_pos[i] * (d_r / 2) + (col - d_c) / 2) * 2;
+      float o0, o1;
+      rope2(v.x, v.y, cs, o0, o1);
+      v = make_float2(o0, o1);
+    }
+    tile[2 * lane][i] = __float2bfloat16_rn(v.x);
+    tile[2 * lane + 1][i] = __float2bfloat16_rn(v.y);
+  }
+  __syncthreads();
+  // lane l writes token t0 + l; element row r of its block lies block_size elements after row r - 1
+  const long long base = dst_base[lane];
+  if (t0 + lane >= T || base < 0) return;
+  for (int r = warp; r < kAppCols; r += 8) {
+    if (c0 + r >= width) break;
+    pool[base + (long long)(c0 + r) * block_size] = tile[r][lane];
   }
 }
 
@@ -465,8 +501,8 @@ cudaError_t tc_compress_append(const Ctx& ctx, const mla_config* cfg, const void
   cudaError_t e = launch_gemm(ctx, a1, a2, b, pl);
   if (e != cudaSuccess) return e;
   const int width = d_c + d_r;
-  dim3 grid(T, (width / 4 + 127) / 128);
-  compress_reduce_kernel<<<grid, 128, 0, ctx.stream>>>(pl.args.partial, pl.args.splits, T, d_c, d_r, seq_idx, pos,
+  dim3 grid((T + kAppTok - 1) / kAppTok, (width + kAppCols - 1) / kAppCols);
+  compress_reduce_kernel<<<grid, 256, 0, ctx.stream>>>(pl.args.partial, pl.args.splits, T, d_c, d_r, seq_idx, pos,
                                                        rope.cos_sin, rope.max_pos, (bf16*)cache.pool,
                                                        cache.num_blocks, cache.block_table, cache.max_blocks_per_seq,
                                                        cache.batch, cfg->block_size, ctx.status);

@@ -92,21 +92,22 @@ __global__ void compress_epilogue_kernel(const float* __restrict__ Y, int T_, in
                                          int block_size, uint32_t* status) {
   const int t = blockIdx.x;
   const int b = seq_idx[t], p = pos[t];
-  long long row = -1;
-  if (b >= 0 && b < batch && p < rope_max) row = cache_row(table, max_blocks, num_blocks, block_size, b, p);
-  if (row < 0) {
+  int blk = -1;
+  if (b >= 0 && b < batch && p < rope_max) blk = cache_block(table, max_blocks, num_blocks, block_size, b, p);
+  if (blk < 0) {
     if (threadIdx.x == 0) flag_error(status, kFlagIndex);
     return;
   }
   const int width = d_c + d_r;
   const float* y = Y + (long long)t * width;
-  T* dst = pool + row * width;
-  for (int i = threadIdx.x; i < d_c; i += blockDim.x) dst[i] = from_f32<T>(y[i]);
+  // element e of this token: pool[(blk * width + e) * block_size + p % block_size]
+  T* dst = pool + (long long)blk * width * block_size + p % block_size;
+  for (int i = threadIdx.x; i < d_c; i += blockDim.x) dst[(long long)i * block_size] = from_f32<T>(y[i]);
   for (int i = threadIdx.x; i < d_r / 2; i += blockDim.x) {
     float o0, o1;
     rope_pair(y[d_c + 2 * i], y[d_c + 2 * i + 1], rope + ((long long)p * (d_r / 2) + i) * 2, o0, o1);
-    dst[d_c + 2 * i] = from_f32<T>(o0);
-    dst[d_c + 2 * i + 1] = from_f32<T>(o1);
+    dst[(long long)(d_c + 2 * i) * block_size] = from_f32<T>(o0);
+    dst[(long long)(d_c + 2 * i + 1) * block_size] = from_f32<T>(o1);
   }
 }
 
@@ -177,14 +178,23 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(
   for (int i = 0; i < kMaxPerLane; ++i) acc[i] = 0.f;
   const int per_lane = (d_c + 31) / 32;
 
+  __shared__ int tile_blk[kChunk];
   for (int t0 = t_begin; t0 < t_end; t0 += kChunk) {
     const int count = min(kChunk, t_end - t0);
     __syncthreads();
-    for (int r = 0; r < count; ++r) {
-      long long row = cache_row(table, max_blocks, num_blocks, block_size, b, t0 + r);
-      if (row < 0 && threadIdx.x == 0) flag_error(status, kFlagIndex);
-      for (int i = threadIdx.x; i < width; i += blockDim.x)
-        tile[r * stride + i] = row < 0 ? 0.f : to_f32<T>(pool[row * width + i]);
+    if (threadIdx.x < count) {
+      const int blk = cache_block(table, max_blocks, num_blocks, block_size, b, t0 + threadIdx.x);
+      if (blk < 0) flag_error(status, kFlagIndex);
+      tile_blk[threadIdx.x] = blk;
+    }
+    __syncthreads();
+    // element i of token r: pool[(blk * width + i) * block_size + (t0 + r) % block_size]
+    for (int idx = threadIdx.x; idx < count * width; idx += blockDim.x) {
+      const int i = idx / count, r = idx % count;
+      const int blk = tile_blk[r];
+      tile[r * stride + i] =
+          blk < 0 ? 0.f
+                  : to_f32<T>(pool[((long long)blk * width + i) * block_size + (t0 + r) % block_size]);
     }
     __syncthreads();
     if (h >= H) continue;

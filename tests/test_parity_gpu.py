@@ -48,7 +48,7 @@ def _stage_decode(dims, dtype, lens, n_q, seed, sharp=1.0, kv_extra=0):
     p = I.make_problem(w, with_weights=False, lens=lens)
     L = Hn.DeviceLayer.__new__(Hn.DeviceLayer)
     L.p, L.device, L.dt, L.cfg = p, DEV, Hn.tdtype(dtype), M.make_config(dims, dtype)
-    L.pool = torch.full((p.num_blocks, dims.block_size, dims.row), float("nan"), dtype=L.dt, device=DEV)
+    L.pool = torch.full((p.num_blocks, dims.row, dims.block_size), float("nan"), dtype=L.dt, device=DEV)
     L.block_table = torch.from_numpy(p.block_table).to(DEV)
     L.cache = M.make_cache(L.pool, L.block_table, dims.block_size)
     L.kv_len = torch.from_numpy(p.kv_len.astype(np.int32)).to(DEV)
