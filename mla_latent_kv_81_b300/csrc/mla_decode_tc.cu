@@ -295,6 +295,27 @@ __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
   asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// ------------------------------------------------------------------ epilogue stores
+// 32 fp32 columns of an O row, normalised, as 4 x 16 bytes of bf16.
+__device__ __forceinline__ void store_bf16_chunk(uint4* dst, const uint32_t (&r)[32], float inv) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 v;
+    v.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv, __uint_as_float(r[8 * i + 1]) * inv);
+    v.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
+    v.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
+    v.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
+    dst[i] = v;
+  }
+}
+// The same columns as fp32 in the partial layout [column / 4][row][4] (dst at this row's first group).
+__device__ __forceinline__ void store_f32_chunk(float4* dst, const uint32_t (&r)[32], float inv) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    dst[(size_t)i * kH] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                      __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+}
+
 // ------------------------------------------------------------------ score MMAs
 // The kE / 16 K-steps of ring slot S of a score tile, each an M = 128 (heads), N = 128 (tokens), K = 16
 // MMA into d: K-step elements e = S * kE + 16 k.  Latent elements take A from the query's TMEM columns
@@ -766,37 +787,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float l = ctrl->l_buf[h], mrow = ctrl->m_buf[h];
           const float inv = l > 0.f ? 1.f / l : 0.f;
           const float lse = l > 0.f ? (mrow + __log2f(l)) * kLn2 : -INFINITY;
+          // eight 32-column chunks of the row, each TMEM load in flight while the previous chunk is stored
+          uint32_t ra[32], rb[32];
+          tmem_ld32(lane_base, ra);
+          tmem_ld_wait();
           if (pc.slot < 0) {
             uint4* dst = reinterpret_cast<uint4*>(p.o_lat + ((size_t)pc.item * kH + h) * kDC + half * 256);
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              uint32_t r[32];
-              tmem_ld32(lane_base + c * 32, r);
+            for (int c = 0; c < 8; c += 2) {
+              tmem_ld32(lane_base + (c + 1) * 32, rb);
+              store_bf16_chunk(dst + c * 4, ra, inv);
               tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv, __uint_as_float(r[8 * i + 1]) * inv);
-                v.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
-                v.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
-                v.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
-                dst[c * 4 + i] = v;
-              }
+              if (c + 2 < 8) tmem_ld32(lane_base + (c + 2) * 32, ra);
+              store_bf16_chunk(dst + (c + 1) * 4, rb, inv);
+              tmem_ld_wait();
             }
             if (p.lse_out && half == 0) p.lse_out[(size_t)pc.item * kH + h] = lse;
           } else {
             // partial layout [slot][column / 4][row][4]: each store of a warp fills 512 contiguous bytes
             float4* dst = reinterpret_cast<float4*>(p.part_o) + ((size_t)pc.slot * (kDC / 4) + half * 64) * kH + h;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              uint32_t r[32];
-              tmem_ld32(lane_base + c * 32, r);
+            for (int c = 0; c < 8; c += 2) {
+              tmem_ld32(lane_base + (c + 1) * 32, rb);
+              store_f32_chunk(dst + (size_t)c * 8 * kH, ra, inv);
               tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[(size_t)(c * 8 + i) * kH] =
-                    make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+              if (c + 2 < 8) tmem_ld32(lane_base + (c + 2) * 32, ra);
+              store_f32_chunk(dst + (size_t)(c + 1) * 8 * kH, rb, inv);
+              tmem_ld_wait();
             }
             if (half == 0) p.part_lse[(size_t)pc.slot * kH + h] = lse;
           }
