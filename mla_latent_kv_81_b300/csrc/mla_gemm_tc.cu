@@ -70,6 +70,9 @@ __device__ __forceinline__ void split_range(const GemmArgs& a, int sp, int& k0, 
   k1 = (int)((long long)(sp + 1) * a.kb / a.splits);
 }
 
+// AMN: A stored [K][M] (M contiguous).  A template parameter so that every MMA operand offset between
+// the MMAs of a k-block is a compile-time constant (runtime arithmetic there stalls their issue).
+template <bool AMN>
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap a_map2,
                    const __grid_constant__ CUtensorMap b_map, GemmArgs a) {
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const bool second = mt >= a.m_tiles1;
           const CUtensorMap* am = second ? &a_map2 : &a_map;
           const int ma = (second ? mt - a.m_tiles1 : mt) * 128;
-          if (a.a_mn) {
+          if (AMN) {
             // A^T stored [K][M]: two [64 k x 64 m] boxes cover the 128 rows of the tile
             tma_load_3d(sa, am, &ctrl->full[st], ma, ka, g);
             tma_load_3d(sa + kATileBytes / 2, am, &ctrl->full[st], ma + 64, ka, g);
@@ -134,7 +137,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, a.n_tile, a.a_mn != 0, false);
+      const uint32_t idesc = idesc_bf16(128, a.n_tile, AMN, false);
+      const uint64_t ring_a = AMN ? desc_sw128(ring_base, kATileBytes / 2, 1024) : desc_sw128(ring_base, 16, 1024);
+      const uint64_t ring_b = desc_sw128(ring_base + kATileBytes, 16, 1024);
+      const uint64_t stage_step = (uint64_t)(a.stage_bytes >> 4);
       int st = 0, acc = 0;
       uint32_t ph = 0, acc_ph = 0;
       for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
@@ -144,18 +150,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (!mbar_wait(&ctrl->acc_empty[acc], acc_ph ^ 1, a.status, abort_flag)) goto done;
         tc_fence_after();
         const uint32_t d = tmem + acc * 256;
+        uint32_t first = 0;   // 0: the unit's first k-block overwrites the accumulator
         for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(&ctrl->full[st], ph, a.status, abort_flag)) goto done;
           tc_fence_after();
-          const uint32_t sa = ring_base + st * a.stage_bytes, sb = sa + kATileBytes;
-          const uint64_t bd = desc_sw128(sb, 16, 1024);
-          const uint64_t ad = a.a_mn ? desc_sw128(sa, kATileBytes / 2, 1024) : desc_sw128(sa, 16, 1024);
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            // K-major operands step 32 B along the swizzled row; an M-major A steps 16 rows of 128 B
-            const uint64_t a_off = a.a_mn ? (uint64_t)(s * (2048 >> 4)) : (uint64_t)(s * 2);
-            mma_ss(d, ad + a_off, bd + (uint64_t)(s * 2), idesc, (kb > k0 || s > 0) ? 1u : 0u);
-          }
+          const uint64_t ad = ring_a + st * stage_step, bd = ring_b + st * stage_step;
+          // K-major operands step 32 B along the swizzled row; an M-major A steps 16 rows of 128 B
+          constexpr uint64_t kAStep = AMN ? (2048 >> 4) : 2;
+          mma_ss(d, ad, bd, idesc, first);
+          mma_ss(d, ad + kAStep, bd + 2, idesc, 1u);
+          mma_ss(d, ad + 2 * kAStep, bd + 4, idesc, 1u);
+          mma_ss(d, ad + 3 * kAStep, bd + 6, idesc, 1u);
+          first = 1;
           mma_commit(&ctrl->empty[st]);
           if (++st == a.stages) { st = 0; ph ^= 1; }
         }
@@ -217,13 +223,6 @@ done:
 }
 
 // ------------------------------------------------------------------ elementwise epilogues
-// Sum of the k-split partials of element (g, n, m).
-__device__ __forceinline__ float sum_splits(const float* part, int splits, long long split_stride, long long idx) {
-  float v = 0.f;
-  for (int s = 0; s < splits; ++s) v += part[s * split_stride + idx];
-  return v;
-}
-
 // Rotate the pair (a, b) by the tabulated angle: (a cos - b sin, a sin + b cos).
 __device__ __forceinline__ void rope2(float a, float b, const float* cs, float& o0, float& o1) {
   o0 = a * cs[0] - b * cs[1];
@@ -283,69 +282,74 @@ __global__ void absorb_reduce_kernel(const float* part, int splits, int N, int H
 
 // Cache rows [c || RoPE(k_R)] from the k-split partials [splits][T][d_c + d_r] of the fused
 // W_DKV / W_KR GEMM, scattered into the paged pool, which stores each block transposed
-// ([d_c + d_r][block_size]).  Block (32-token group, 64-column group): the partials are read token by
-// token (coalesced), summed, rotated and rounded, transposed through shared memory and written column
-// by column, so that tokens at consecutive positions of one block write contiguous bytes.
-constexpr int kAppTok = 32, kAppCols = 64;
+// ([d_c + d_r][block_size]).  Block (8-token group, 64-column group), warp w = token t0 + w: the partials
+// are read token by token (coalesced, all splits in flight at once), summed, rotated and rounded, then
+// transposed through shared memory so that tokens at consecutive positions of one block write
+// contiguous bytes of each element row.
+constexpr int kAppTok = 8, kAppCols = 64;
 
 __global__ void __launch_bounds__(256) compress_reduce_kernel(const float* part, int splits, int T, int d_c, int d_r,
                                                               const int32_t* seq_idx, const int32_t* pos,
                                                               const float* rope, int rope_max, bf16* pool,
                                                               int num_blocks, const int32_t* table, int max_blocks,
                                                               int batch, int block_size, uint32_t* status) {
-  __shared__ bf16 tile[kAppCols][kAppTok + 2];
+  __shared__ bf16 tile[kAppCols][kAppTok];
   __shared__ long long dst_base[kAppTok];   // pool offset of column 0 of each token, or -1 (skipped)
-  __shared__ int tok_pos[kAppTok];
   const int t0 = blockIdx.x * kAppTok, c0 = blockIdx.y * kAppCols;
   const int width = d_c + d_r;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x < kAppTok) {
-    const int t = t0 + threadIdx.x;
-    long long base = -1;
-    int p = 0;
-    if (t < T) {
-      const int b = seq_idx[t];
-      p = pos[t];
-      int blk = -1;
-      if (b >= 0 && b < batch && p >= 0 && p < rope_max)
-        blk = cache_block(table, max_blocks, num_blocks, block_size, b, p);
-      if (blk < 0) {
-        if (blockIdx.y == 0) flag_error(status, kFlagIndex);
-      } else {
-        base = (long long)blk * width * block_size + p % block_size;
+  const int t = t0 + warp;
+  // lane l holds columns c0 + 2l and c0 + 2l + 1 of token t (a RoPE pair when in the k_R part)
+  const int col = c0 + 2 * lane;
+  int p_t = 0;
+  long long base = -1;
+  if (t < T) {
+    const int b = seq_idx[t];
+    p_t = pos[t];
+    int blk = -1;
+    if (b >= 0 && b < batch && p_t >= 0 && p_t < rope_max)
+      blk = cache_block(table, max_blocks, num_blocks, block_size, b, p_t);
+    if (blk < 0) {
+      if (blockIdx.y == 0 && lane == 0) flag_error(status, kFlagIndex);
+    } else {
+      base = (long long)blk * width * block_size + p_t % block_size;
+    }
+  }
+  if (lane == 0) dst_base[warp] = base;
+  if (base >= 0 && col < width) {
+    const long long idx = (long long)t * width + col, sstride = (long long)T * width;
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    int sp = 0;
+    for (; sp + 4 <= splits; sp += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 w = *reinterpret_cast<const float2*>(part + (sp + u) * sstride + idx);
+        acc[u].x += w.x;
+        acc[u].y += w.y;
       }
     }
-    dst_base[threadIdx.x] = base;
-    tok_pos[threadIdx.x] = p;
-  }
-  __syncthreads();
-  // lane l holds columns c0 + 2l and c0 + 2l + 1 of token i (a RoPE pair when in the k_R part)
-  const int col = c0 + 2 * lane;
-  for (int i = warp; i < kAppTok; i += 8) {
-    if (t0 + i >= T || col >= width || dst_base[i] < 0) continue;
-    const long long idx = (long long)(t0 + i) * width + col;
-    float2 v = *reinterpret_cast<const float2*>(part + idx);
-    for (int sp = 1; sp < splits; ++sp) {
-      const float2 w = *reinterpret_cast<const float2*>(part + (long long)sp * T * width + idx);
-      v.x += w.x;
-      v.y += w.y;
+    for (; sp < splits; ++sp) {
+      const float2 w = *reinterpret_cast<const float2*>(part + sp * sstride + idx);
+      acc[0].x += w.x;
+      acc[0].y += w.y;
     }
+    float2 v = make_float2((acc[0].x + acc[1].x) + (acc[2].x + acc[3].x), (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y));
     if (col >= d_c) {
-      const float* cs = rope + ((long long)tok_pos[i] * (d_r / 2) + (col - d_c) / 2) * 2;
+      const float* cs = rope + ((long long)p_t * (d_r / 2) + (col - d_c) / 2) * 2;
       float o0, o1;
       rope2(v.x, v.y, cs, o0, o1);
       v = make_float2(o0, o1);
     }
-    tile[2 * lane][i] = __float2bfloat16_rn(v.x);
-    tile[2 * lane + 1][i] = __float2bfloat16_rn(v.y);
+    tile[2 * lane][warp] = __float2bfloat16_rn(v.x);
+    tile[2 * lane + 1][warp] = __float2bfloat16_rn(v.y);
   }
   __syncthreads();
-  // lane l writes token t0 + l; element row r of its block lies block_size elements after row r - 1
-  const long long base = dst_base[lane];
-  if (t0 + lane >= T || base < 0) return;
-  for (int r = warp; r < kAppCols; r += 8) {
-    if (c0 + r >= width) break;
-    pool[base + (long long)(c0 + r) * block_size] = tile[r][lane];
+  // thread (r, j): element row c0 + r of token t0 + j
+#pragma unroll
+  for (int k = 0; k < kAppCols * kAppTok / 256; ++k) {
+    const int e = threadIdx.x + k * 256, r = e / kAppTok, j = e % kAppTok;
+    const long long bj = dst_base[j];
+    if (t0 + j < T && bj >= 0 && c0 + r < width) pool[bj + (long long)(c0 + r) * block_size] = tile[r][j];
   }
 }
 
@@ -444,10 +448,14 @@ size_t partial_bytes(const GemmPlan& p) {
 cudaError_t launch_gemm(const Ctx& ctx, const CUtensorMap& am, const CUtensorMap& am2, const CUtensorMap& bm,
                         GemmPlan& p) {
   p.args.status = ctx.status;
-  cudaError_t e = ensure_smem_limit((const void*)gemm_tc_kernel, kGSmem, ctx.device);
+  const void* kern = p.args.a_mn ? (const void*)gemm_tc_kernel<true> : (const void*)gemm_tc_kernel<false>;
+  cudaError_t e = ensure_smem_limit(kern, kGSmem, ctx.device);
   if (e != cudaSuccess) return e;
   if (p.args.units == 0) return cudaSuccess;
-  gemm_tc_kernel<<<p.grid, kGThreads, kGSmem, ctx.stream>>>(am, am2, bm, p.args);
+  if (p.args.a_mn)
+    gemm_tc_kernel<true><<<p.grid, kGThreads, kGSmem, ctx.stream>>>(am, am2, bm, p.args);
+  else
+    gemm_tc_kernel<false><<<p.grid, kGThreads, kGSmem, ctx.stream>>>(am, am2, bm, p.args);
   count_launch();
   return cudaGetLastError();
 }
