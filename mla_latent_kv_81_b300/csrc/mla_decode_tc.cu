@@ -31,6 +31,7 @@
 // of all queries are cut into equal contiguous ranges, one per cluster
 // (split-KV); ranges that cover part of a query write fp32 partials that a
 // second kernel, launched as a programmatic dependent, merges by log-sum-exp.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include <mutex>
@@ -123,7 +124,7 @@ struct Params {
   int* prefix;                // [items + 1]: exclusive prefix of visible tiles (written by CTA 0)
   bf16* o_lat;
   float* lse_out;
-  float* part_o;
+  __half* part_o;               // [2 clusters][kDC / 8][kH][8] fp16
   float* part_lse;
   float scale_log2;
   uint32_t* status;
@@ -308,12 +309,24 @@ __device__ __forceinline__ void store_bf16_chunk(uint4* dst, const uint32_t (&r)
     dst[i] = v;
   }
 }
-// The same columns as fp32 in the partial layout [column / 4][row][4] (dst at this row's first group).
-__device__ __forceinline__ void store_f32_chunk(float4* dst, const uint32_t (&r)[32], float inv) {
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The same columns as fp16 in the partial layout [column / 8][row][8] (dst at this row's first group): a
+// partial is a normalised weighted mean of cached values, well inside fp16 range, and 11 significant
+// bits keep its rounding far below the bf16 rounding of the final output.
+__device__ __forceinline__ void store_f16_chunk(uint4* dst, const uint32_t (&r)[32], float inv) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    dst[(size_t)i * kH] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                      __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+  for (int i = 0; i < 4; ++i) {
+    uint4 v;
+    v.x = pack_f16x2(__uint_as_float(r[8 * i + 0]) * inv, __uint_as_float(r[8 * i + 1]) * inv);
+    v.y = pack_f16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
+    v.z = pack_f16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
+    v.w = pack_f16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
+    dst[(size_t)i * kH] = v;
+  }
 }
 
 // ------------------------------------------------------------------ score MMAs
@@ -804,15 +817,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (p.lse_out && half == 0) p.lse_out[(size_t)pc.item * kH + h] = lse;
           } else {
-            // partial layout [slot][column / 4][row][4]: each store of a warp fills 512 contiguous bytes
-            float4* dst = reinterpret_cast<float4*>(p.part_o) + ((size_t)pc.slot * (kDC / 4) + half * 64) * kH + h;
+            // partial layout [slot][column / 8][row][8] (fp16): each store of a warp fills 512 contiguous bytes
+            uint4* dst = reinterpret_cast<uint4*>(p.part_o) + ((size_t)pc.slot * (kDC / 8) + half * 32) * kH + h;
 #pragma unroll 1
             for (int c = 0; c < 8; c += 2) {
               tmem_ld32(lane_base + (c + 1) * 32, rb);
-              store_f32_chunk(dst + (size_t)c * 8 * kH, ra, inv);
+              store_f16_chunk(dst + (size_t)c * 4 * kH, ra, inv);
               tmem_ld_wait();
               if (c + 2 < 8) tmem_ld32(lane_base + (c + 2) * 32, ra);
-              store_f32_chunk(dst + (size_t)(c + 1) * 8 * kH, rb, inv);
+              store_f16_chunk(dst + (size_t)(c + 1) * 4 * kH, rb, inv);
               tmem_ld_wait();
             }
             if (half == 0) p.part_lse[(size_t)pc.slot * kH + h] = lse;
@@ -846,7 +859,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // nothing visible, were written by the attention kernel itself.
 constexpr int kMergeGroups = kDC / 16;
 
-__global__ void __launch_bounds__(kH) merge_kernel(const int* prefix, int items, int clusters, const float* part_o,
+__global__ void __launch_bounds__(kH) merge_kernel(const int* prefix, int items, int clusters, const __half* part_o,
                                                    const float* part_lse, bf16* o_lat, float* lse_out) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int item = blockIdx.x, g = blockIdx.y, h = threadIdx.x;
@@ -866,15 +879,18 @@ __global__ void __launch_bounds__(kH) merge_kernel(const int* prefix, int items,
     const int slot = c == c0 ? 2 * c + 1 : 2 * c;
     const float w = expf(part_lse[(size_t)slot * kH + h] - mx);
     z += w;
-    // partial layout [slot][column / 4][row][4]
-    const float4* src = reinterpret_cast<const float4*>(part_o) + ((size_t)slot * (kDC / 4) + g * 4) * kH + h;
+    // partial layout [slot][column / 8][row][8] (fp16)
+    const uint4* src = reinterpret_cast<const uint4*>(part_o) + ((size_t)slot * (kDC / 8) + g * 2) * kH + h;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float4 v = src[(size_t)j * kH];
-      acc[4 * j] = fmaf(w, v.x, acc[4 * j]);
-      acc[4 * j + 1] = fmaf(w, v.y, acc[4 * j + 1]);
-      acc[4 * j + 2] = fmaf(w, v.z, acc[4 * j + 2]);
-      acc[4 * j + 3] = fmaf(w, v.w, acc[4 * j + 3]);
+    for (int j = 0; j < 2; ++j) {
+      const uint4 v = src[(size_t)j * kH];
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[q]));
+        acc[8 * j + 2 * q] = fmaf(w, f.x, acc[8 * j + 2 * q]);
+        acc[8 * j + 2 * q + 1] = fmaf(w, f.y, acc[8 * j + 2 * q + 1]);
+      }
     }
   }
   const float inv = 1.f / z;
@@ -950,7 +966,7 @@ WsLayout ws_layout(int items, int C) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = (o + bytes + 255) / 256 * 256; return r; };
   w.prefix = take(sizeof(int) * (items + 1));
-  w.part_o = take(sizeof(float) * (size_t)2 * C * kH * kDC);
+  w.part_o = take(sizeof(__half) * (size_t)2 * C * kH * kDC);
   w.part_lse = take(sizeof(float) * (size_t)2 * C * kH);
   w.total = o;
   return w;
@@ -1015,7 +1031,7 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   prm.prefix = reinterpret_cast<int*>(ws + w.prefix);
   prm.o_lat = static_cast<bf16*>(o_lat);
   prm.lse_out = lse;
-  prm.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  prm.part_o = reinterpret_cast<__half*>(ws + w.part_o);
   prm.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
   prm.scale_log2 = scale * kLog2e;
   prm.status = ctx.status;
@@ -1038,7 +1054,7 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   at[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, merge_kernel, (const int*)prm.prefix, items, C, (const float*)prm.part_o,
+  e = cudaLaunchKernelEx(&lc, merge_kernel, (const int*)prm.prefix, items, C, (const __half*)prm.part_o,
                          (const float*)prm.part_lse, prm.o_lat, lse);
   count_launch();
   if (e != cudaSuccess) return e;
