@@ -384,7 +384,7 @@ def run_ours(args, rank: int, world: int):
         roof = {"bound": "tensor", "achieved": ach_tf, "peak": tf_peak, "unit": "TFLOP/s", "frac": ach_tf / tf_peak}
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
     roof["traffic"] = recorded_traffic(w.name)
-    roof["kernel"] = ("mla_decode_attention (planner, attention and split-KV merge launches, replayed as one CUDA "
+    roof["kernel"] = ("mla_decode_attention (attention and split-KV merge launches, replayed as one CUDA "
                       "graph), CUDA events on its stream")
     roof["ms_per_launch"] = dec_mean
     roof["algorithmic_bytes_per_launch"] = alg["bytes"]
@@ -417,7 +417,7 @@ def run_ours(args, rank: int, world: int):
 
 
 def run_sweep(args):
-    """One JSON line per workload: the decode call (planner + attention + merge) as the median of
+    """One JSON line per workload: the decode call (attention + merge) as the median of
     `--sweep-reps` runs with L2 flushed before each (a 256 MB write outside the timed region), its
     cached tokens/s, algorithmic GB/s and roofline fraction, and the projection calls timed the same way."""
     import torch

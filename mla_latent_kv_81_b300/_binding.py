@@ -101,7 +101,7 @@ def _check(fn: str, code: int):
 
 
 def make_cache(pool, block_table, block_size: int) -> mla_paged_cache:
-    """pool: [num_blocks, block_size, d_c + d_rope]; block_table: int32 [batch, max_blocks]."""
+    """pool: [num_blocks, d_c + d_rope, block_size] (element-major blocks); block_table: int32 [batch, max_blocks]."""
     return mla_paged_cache(pool.data_ptr(), pool.shape[0], block_table.data_ptr(), block_table.shape[1],
                            block_table.shape[0])
 
