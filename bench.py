@@ -478,6 +478,62 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def prefill_algorithmic(c: I.PrefillCase) -> dict:
+    """Work of one mla_prefill_attention call in the explicit form: the per-head keys and values rebuilt
+    for every cached token (2 d_c (qk_nope + v_head) FLOP per token and head), and for every (query,
+    visible key, head) 2 (qk_nope + d_rope) FLOP of score and 2 v_head of P V.  Bytes: the latent rows,
+    the up-projections, the queries and the outputs."""
+    d = c.dims
+    H, L, T = d.n_heads, c.prompt, c.queries
+    pairs = sum(L - T + j + 1 for j in range(T))
+    flops = 2.0 * L * d.d_c * H * (d.qk_nope + d.v_head) + 2.0 * pairs * H * (d.qk_nope + d.d_rope + d.v_head)
+    nbytes = 2.0 * (L * d.row + H * (d.qk_nope + d.v_head) * d.d_c + T * H * (d.qk_nope + d.d_rope) + T * H * d.v_head)
+    return {"flops": flops, "bytes": nbytes, "pairs": pairs}
+
+
+def run_prefill(args):
+    """One JSON line per prefill case: the explicit-form attention call (latent gather, K/V GEMM,
+    attention kernel) as the median of `--sweep-reps` runs with L2 flushed before each, its TFLOP/s and
+    the fraction of the tensor roofline."""
+    import torch
+    import mla_harness as Hn
+
+    hbm_peak, tf_peak, peak_kind = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for name in args.prefill_cases.split(","):
+        c = I.PREFILL_CASES[name]
+        p = I.make_prefill(c)
+        L = Hn.PrefillLayer(p)
+        L.fill()
+        for _ in range(3):
+            L.attend(with_lse=False)
+        ts = []
+        for _ in range(args.sweep_reps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            L.attend(with_lse=False)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        code, flags = L.status()
+        if code != 0:
+            raise RuntimeError(f"{name}: device status {code} ({flags})")
+        t = statistics.median(ts)
+        alg = prefill_algorithmic(c)
+        t_tc, t_hbm = alg["flops"] / (tf_peak * 1e12), alg["bytes"] / (hbm_peak * 1e9)
+        print(json.dumps({
+            "prefill": name, "dtype": c.dtype, "prompt": c.prompt, "queries": c.queries, "call_ms": t,
+            "achieved_tflops": alg["flops"] / (t * 1e-3) / 1e12,
+            "roofline": {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_roof_ms": max(t_tc, t_hbm) * 1e3,
+                         "frac": max(t_tc, t_hbm) / (t * 1e-3),
+                         "peaks": f"{peak_kind}: {hbm_peak} GB/s, {tf_peak} TFLOP/s bf16"},
+            "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
+            "timing": f"median of {args.sweep_reps}, L2 flushed (256 MB write) before each"}), flush=True)
+        del L
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,6 +546,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the step benchmark, one JSON line per workload (decode call and projections)")
     ap.add_argument("--sweep-reps", type=int, default=50)
+    ap.add_argument("--prefill", action="store_true",
+                    help="instead of the step benchmark, one JSON line per prefill case (explicit-form attention)")
+    ap.add_argument("--prefill-cases", default="prefill_dsv2_L4096_T4096,prefill_dsv2_L8192_T8192")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -498,6 +557,9 @@ def main():
     if args.sweep:
         if rank == 0:
             run_sweep(args)
+    elif args.prefill:
+        if rank == 0:
+            run_prefill(args)
     elif args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -182,10 +182,9 @@ size_t mla_decode_workspace_bytes(const mla_config* cfg, int batch, int n_q, int
  *           visible), or NULL
  * A query with no visible token gets o_lat = 0.
  * Reproducibility: on the tensor-core path each 128-token score tile sums its
- * nine 64-element chunks in the order their loads complete, so two calls on
- * the same inputs may differ in the last bits of the fp32 scores (and, through
- * bf16 rounding of P and o_lat, by up to about one bf16 ulp); the result is
- * otherwise independent of how the sequences are split across CTAs. */
+ * six 96-element slices in a fixed order, so repeated calls on the same inputs
+ * and GPU give the same bits; another SM count or batch moves the split points
+ * and changes results only by fp32 rounding. */
 mla_status mla_decode_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache,
                                 const int32_t* kv_len, int batch, int n_q, void* o_lat, float* lse,
                                 void* workspace, size_t workspace_bytes, mla_stream_t stream);
@@ -202,6 +201,66 @@ size_t mla_output_workspace_bytes(const mla_config* cfg, int N);
 mla_status mla_output_project(const mla_config* cfg, const void* o_lat, const void* W_UV, const void* W_O,
                               void* out, int N, void* workspace, size_t workspace_bytes,
                               mla_stream_t stream);
+
+/* ---- Explicit form: prefill of a prompt (keys and values rebuilt per head) ----
+ * At prefill every prompt token is a query.  Rebuilding the per-head keys and
+ * values from the cached latent ([TM] point 4: K/V recomputed from the latent at
+ * prefill; [KJ "The mechanism"]: up-projections expand the latent into per-head
+ * keys and values) costs 2 (qk_nope + d_rope + v_head) FLOP per (query, key,
+ * head) against 2 (2 d_c + d_rope) for the absorbed form, so long prompts take
+ * this path: mla_project_query, mla_prefill_attention, mla_head_output_project.
+ * bf16 only, on the tensor-core shapes above; fp32 returns MLA_ERR_UNSUPPORTED. */
+
+/* Workspace bytes mla_project_query needs for N query tokens. */
+size_t mla_project_workspace_bytes(const mla_config* cfg, int N);
+
+/* Project N query tokens without absorbing W_UK:
+ *   q_nope^h = W_Q^h x,  q_R^h = RoPE(W_QR^h x, q_pos)
+ *   x      device [N][d_model];  q_pos device int32 [N]
+ *   W_Q    device [n_heads*qk_nope][d_model];  W_QR device [n_heads*d_rope][d_model]
+ *   q_out  device [N][n_heads][qk_nope + d_rope] = [q_nope^h || q_R^h]
+ * A q_pos outside the RoPE table skips that token's rotated part and is flagged. */
+mla_status mla_project_query(const mla_config* cfg, const void* x, const void* W_Q, const void* W_QR,
+                             const int32_t* q_pos, const mla_rope_table* rope, void* q_out, int N,
+                             void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* Workspace bytes mla_prefill_attention needs for a sequence of kv_len cached
+ * tokens: the 256-byte header, the sequence's latent rows token-major
+ * (kv_len * (d_c + d_rope) bf16) and its rebuilt keys and values
+ * (kv_len * n_heads * (qk_nope + v_head) bf16, 64 KB per token at the
+ * DeepSeek-V2 shape). */
+size_t mla_prefill_workspace_bytes(const mla_config* cfg, int kv_len);
+
+/* Causal attention of the last T tokens of sequence `seq` over its first kv_len
+ * cached tokens, in the explicit form:
+ *   k_t^h = [W_UK^h c_t || k_R,t],  v_t^h = W_UV^h c_t                 ([BB "1. Low-Rank
+ *                                     Decomposition"], names read as up-projections)
+ *   s_t^h = scale * (q_nope^h . W_UK^h c_t + q_R^h . k_R,t)  for t <= pos_j
+ *   o^h   = sum_t softmax(s^h)_t v_t^h
+ * Query j (0 <= j < T) has position pos_j = kv_len - T + j and sees tokens 0..pos_j
+ * ([SC]: every prior token keeps an entry).  Its rows must already be in the
+ * cache (mla_compress_append of the prompt).
+ *   q      device [T][n_heads][qk_nope + d_rope] (mla_project_query output)
+ *   cache  the paged cache; seq < cache->batch; kv_len <= max_blocks_per_seq * block_size
+ *   W_UK   device [n_heads][qk_nope][d_c];  W_UV device [n_heads][v_head][d_c]
+ *   o      device [T][n_heads][v_head]
+ *   lse    optional device fp32 [T][n_heads] (natural log of the softmax
+ *          normaliser of the scaled scores), or NULL
+ * 1 <= T <= kv_len.  Block-table entries outside the pool read as zero rows
+ * and are flagged.  Three launches: the latent gather, the K/V GEMM, the
+ * attention kernel. */
+mla_status mla_prefill_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache, int seq,
+                                 int kv_len, int T, const void* W_UK, const void* W_UV, void* o, float* lse,
+                                 void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* Workspace bytes mla_head_output_project needs for N tokens. */
+size_t mla_head_output_workspace_bytes(const mla_config* cfg, int N);
+
+/* The output projection of per-head outputs: out = W_O concat_h(o^h).
+ *   o    device [N][n_heads][v_head];  W_O device [d_model][n_heads*v_head]
+ *   out  device [N][d_model] */
+mla_status mla_head_output_project(const mla_config* cfg, const void* o, const void* W_O, void* out, int N,
+                                   void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /* Synchronise `stream`, then read and clear the status word of `workspace`
  * (the word in its header), or, when workspace is NULL, the library's own word

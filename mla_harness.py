@@ -154,3 +154,98 @@ class DeviceLayer:
         """Rows 0..n-1 of sequence b read back from the pool, as float32 numpy (exact bf16 values)."""
         n = int(self.p.kv_len[b]) if n is None else n
         return self.cache_rows_at(np.full(n, b), np.arange(n))
+
+
+def write_rows(pool, block_table: np.ndarray, b: int, rows, block_size: int):
+    """Store token-major rows [n, row] at positions 0..n-1 of sequence b of an element-major pool."""
+    n = rows.shape[0]
+    n_full = n // block_size
+    if n_full:
+        blks = torch.from_numpy(block_table[b, :n_full].astype(np.int64)).to(pool.device)
+        pool[blks] = rows[:n_full * block_size].reshape(n_full, block_size, rows.shape[1]).transpose(1, 2)
+    rem = n - n_full * block_size
+    if rem:
+        pool[int(block_table[b, n_full]), :, :rem] = rows[n_full * block_size:].T
+
+
+class PrefillLayer:
+    """A prompt on the device (mla_inputs.PrefillProblem) and the explicit-form calls over it."""
+
+    def __init__(self, p: I.PrefillProblem, device="cuda"):
+        self.p = p
+        c, d = p.case, p.dims
+        self.device = device
+        self.dt = tdtype(c.dtype)
+        self.cfg = M.make_config(d, c.dtype)
+        self.W = {k: to_dev(v, c.dtype, device) for k, v in p.weights.items()}
+        self.pool = torch.full((p.num_blocks, d.row, d.block_size), float("nan"), dtype=self.dt, device=device)
+        self.block_table = torch.from_numpy(p.block_table).to(device)
+        self.cache = M.make_cache(self.pool, self.block_table, d.block_size)
+        max_pos = int(p.block_table.shape[1]) * d.block_size + 8
+        self.rope_tab = torch.empty((max_pos, d.d_rope // 2, 2), dtype=torch.float32, device=device)
+        M.mla_rope_table_create(self.cfg, d.rope_base, max_pos, self.rope_tab)
+        self.rope = M.make_rope(self.rope_tab)
+        T = c.queries
+        self.q = (to_dev(p.q, c.dtype, device) if p.q is not None else
+                  torch.empty((T, d.n_heads, d.qk_nope + d.d_rope), dtype=self.dt, device=device))
+        self.o = torch.empty((T, d.n_heads, d.v_head), dtype=self.dt, device=device)
+        self.lse = torch.empty((T, d.n_heads), dtype=torch.float32, device=device)
+        self.out = torch.empty((T, d.d_model), dtype=self.dt, device=device)
+        self.ws = {}
+        if p.x is not None:
+            self.x = to_dev(p.x, c.dtype, device)
+
+    def _ws(self, key, nbytes):
+        t = self.ws.get(key)
+        if t is None or t.numel() < nbytes:
+            t = M.workspace(nbytes, self.device)
+            self.ws[key] = t
+        return t
+
+    def status(self, stream=None):
+        flags = 0
+        for t in self.ws.values():
+            _, f = M.mla_get_device_status(t, stream)
+            flags |= f
+        return (5 if flags & 1 else 4 if flags & 2 else 0), flags
+
+    def fill(self):
+        """Cache rows of the prompt: drawn rows written directly, or appended from the hidden states."""
+        p, c, d = self.p, self.p.case, self.p.dims
+        if p.rows is not None:
+            write_rows(self.pool, p.block_table, c.seq, to_dev(p.rows, c.dtype, self.device), d.block_size)
+            return
+        L = c.prompt
+        seq = torch.full((L,), c.seq, dtype=torch.int32, device=self.device)
+        pos = torch.arange(L, dtype=torch.int32, device=self.device)
+        ws = self._ws("fill", M.mla_compress_workspace_bytes(self.cfg, L))
+        M.mla_compress_append(self.cfg, self.x, self.W["W_DKV"], self.W["W_KR"], seq, pos, self.rope, self.cache,
+                              ws=ws)
+
+    def project(self, stream=None):
+        """Queries [q_nope || q_R] of the last `queries` prompt tokens from their hidden states."""
+        c = self.p.case
+        xq = self.x[c.prompt - c.queries:]
+        q_pos = torch.from_numpy(self.p.q_pos).to(self.device)
+        ws = self._ws("q", M.mla_project_workspace_bytes(self.cfg, c.queries))
+        M.mla_project_query(self.cfg, xq, self.W["W_Q"], self.W["W_QR"], q_pos, self.rope, self.q, ws=ws,
+                            stream=stream)
+        return self.q
+
+    def attend(self, stream=None, with_lse=True):
+        c = self.p.case
+        ws = self._ws("p", M.mla_prefill_workspace_bytes(self.cfg, c.prompt))
+        M.mla_prefill_attention(self.cfg, self.q, self.cache, c.seq, c.prompt, self.W["W_UK"], self.W["W_UV"],
+                                self.o, self.lse if with_lse else None, ws=ws, stream=stream)
+        return self.o
+
+    def output(self, stream=None):
+        ws = self._ws("o", M.mla_head_output_workspace_bytes(self.cfg, self.p.case.queries))
+        M.mla_head_output_project(self.cfg, self.o, self.W["W_O"], self.out, ws=ws, stream=stream)
+        return self.out
+
+    def run(self, stream=None):
+        """The explicit-form layer from hidden states: queries, attention, output projection."""
+        self.project(stream)
+        self.attend(stream)
+        return self.output(stream)

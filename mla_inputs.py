@@ -226,6 +226,87 @@ def paged_slots(block_table: np.ndarray, b: int, positions: np.ndarray, block_si
     return block_table[b, positions // block_size].astype(np.int64) * block_size + positions % block_size
 
 
+# ---------------------------------------------------------------- prefill (explicit form)
+@dataclass(frozen=True)
+class PrefillCase:
+    """A prompt of `prompt` tokens (positions 0..prompt-1) held by sequence `seq` of a small batch whose
+    other sequences hold `others` tokens each: their blocks interleave with the prompt's in the shuffled
+    block table and stay unwritten (NaN sentinels).  The last `queries` prompt tokens are the queries.
+    fill "direct": cache rows and queries [q_nope || q_R] are drawn directly (the attention stage alone);
+    fill "append": the prompt's hidden states are drawn and everything else is computed from them."""
+    name: str
+    dims: Dims
+    dtype: str
+    prompt: int
+    queries: int
+    seed: int
+    fill: str = "direct"
+    others: tuple = (100, 37)
+    seq: int = 1
+    note: str = ""
+
+
+PREFILL_CASES = {
+    c.name: c
+    for c in [
+        PrefillCase("prefill_dsv2_L300_T300", DSV2, "bf16", 300, 300, 40, note="whole prompt, ragged tiles"),
+        PrefillCase("prefill_dsv2_L700_T200", DSV2, "bf16", 700, 200, 41,
+                    note="the last 200 tokens of 700: query tiles straddle key tiles"),
+        PrefillCase("prefill_dsv2_L300_T1", DSV2, "bf16", 300, 1, 42, note="one query"),
+        PrefillCase("prefill_dsv2_L64_T64", DSV2, "bf16", 64, 64, 43, note="one cache block"),
+        PrefillCase("prefill_dsv2_L1_T1", DSV2, "bf16", 1, 1, 44, others=(5,), seq=0, note="a single token"),
+        PrefillCase("prefill_dsv2_L333_T333_x", DSV2, "bf16", 333, 333, 45, fill="append",
+                    note="from hidden states: append, query projection, attention, output projection"),
+        PrefillCase("prefill_dsv2_L4096_T4096", DSV2, "bf16", 4096, 4096, 46,
+                    note="a 4096-token prompt (benchmark size)"),
+        PrefillCase("prefill_dsv2_L8192_T8192", DSV2, "bf16", 8192, 8192, 47, note="an 8192-token prompt"),
+    ]
+}
+
+
+@dataclass
+class PrefillProblem:
+    case: PrefillCase
+    weights: dict
+    x: np.ndarray | None        # [prompt, d_model] hidden states (fill "append")
+    rows: np.ndarray | None     # [prompt, d_c + d_rope] cache rows (fill "direct")
+    q: np.ndarray | None        # [queries, H, qk_nope + d_rope] queries (fill "direct")
+    lens: np.ndarray            # cached tokens of every sequence of the batch
+    block_table: np.ndarray
+    num_blocks: int
+
+    @property
+    def dims(self) -> Dims:
+        return self.case.dims
+
+    @property
+    def q_pos(self) -> np.ndarray:
+        return np.arange(self.case.prompt - self.case.queries, self.case.prompt, dtype=np.int32)
+
+
+def make_prefill(c: PrefillCase, sharp: float = 1.0) -> PrefillProblem:
+    """Draw a prefill case: main stream seeded with c.seed; weights, then the hidden states (append) or
+    the cache rows and queries (direct, queries scaled by `sharp` before rounding), then the block
+    permutation."""
+    rng = np.random.default_rng(c.seed)
+    d = c.dims
+    weights = draw_weights(d, c.dtype, rng)
+    x = rows = q = None
+    if c.fill == "append":
+        x = draw_hidden(rng, c.prompt, d.d_model, c.dtype)
+    else:
+        rows = storage(_normal(rng, (c.prompt, d.row), 1.0), c.dtype)
+        qq = _normal(rng, (c.queries, d.n_heads, d.qk_nope + d.d_rope), 1.0)
+        if sharp != 1.0:
+            qq *= np.float32(sharp)
+        q = storage(qq, c.dtype)
+    lens = list(c.others)
+    lens.insert(c.seq, c.prompt)
+    lens = np.asarray(lens, dtype=np.int64)
+    table, num_blocks = draw_block_table(lens, d.block_size, rng)
+    return PrefillProblem(c, weights, x, rows, q, lens, table, num_blocks)
+
+
 # ---------------------------------------------------------------- stage inputs
 def draw_stage_query(dims: Dims, dtype: str, n: int, seed: int, sharp: float = 1.0) -> np.ndarray:
     """Absorbed query rows [n, H, d_c + d_rope] drawn directly, for testing attention alone.

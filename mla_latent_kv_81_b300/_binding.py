@@ -63,6 +63,12 @@ def _load():
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_kernel_launches": (ctypes.c_uint64, []),
         "mla_compress_append_noalloc": (I, [cfgp, VP, VP, VP, VP, VP, ropep, cachep, I, VP]),
+        "mla_project_workspace_bytes": (Z, [cfgp, I]),
+        "mla_project_query": (I, [cfgp, VP, VP, VP, VP, ropep, VP, I, VP, Z, VP]),
+        "mla_prefill_workspace_bytes": (Z, [cfgp, I]),
+        "mla_prefill_attention": (I, [cfgp, VP, cachep, I, I, I, VP, VP, VP, VP, VP, Z, VP]),
+        "mla_head_output_workspace_bytes": (Z, [cfgp, I]),
+        "mla_head_output_project": (I, [cfgp, VP, VP, VP, I, VP, Z, VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -75,7 +81,9 @@ EXPORTED = ("mla_cache_bytes_per_token", "mla_rope_table_create", "mla_compress_
             "mla_compress_append", "mla_absorb_workspace_bytes", "mla_absorb_query",
             "mla_decode_workspace_bytes", "mla_decode_attention", "mla_output_workspace_bytes",
             "mla_output_project", "mla_get_device_status", "mla_status_string", "mla_kernel_launches",
-            "mla_compress_append_noalloc", "mla_selftest_wait_timeout")
+            "mla_compress_append_noalloc", "mla_selftest_wait_timeout", "mla_project_workspace_bytes",
+            "mla_project_query", "mla_prefill_workspace_bytes", "mla_prefill_attention",
+            "mla_head_output_workspace_bytes", "mla_head_output_project")
 
 
 # ------------------------------------------------------------------ marshalling helpers
@@ -191,6 +199,49 @@ def mla_output_project(cfg, o_lat, W_UV, W_O, out, ws=None, stream=None):
     _check("mla_output_project",
            lib.mla_output_project(ctypes.byref(cfg), _ptr(o_lat), _ptr(W_UV), _ptr(W_O), _ptr(out), N, _ptr(ws),
                                   ws.numel(), _stream(stream)))
+    return out
+
+
+def mla_project_workspace_bytes(cfg, N):
+    return int(lib.mla_project_workspace_bytes(ctypes.byref(cfg), N))
+
+
+def mla_project_query(cfg, x, W_Q, W_QR, q_pos, rope: mla_rope_table, q_out, ws=None, stream=None):
+    N = x.shape[0]
+    if ws is None:
+        ws = workspace(mla_project_workspace_bytes(cfg, N), x.device)
+    _check("mla_project_query",
+           lib.mla_project_query(ctypes.byref(cfg), _ptr(x), _ptr(W_Q), _ptr(W_QR), _ptr(q_pos), ctypes.byref(rope),
+                                 _ptr(q_out), N, _ptr(ws), ws.numel(), _stream(stream)))
+    return q_out
+
+
+def mla_prefill_workspace_bytes(cfg, kv_len):
+    return int(lib.mla_prefill_workspace_bytes(ctypes.byref(cfg), kv_len))
+
+
+def mla_prefill_attention(cfg, q, cache: mla_paged_cache, seq, kv_len, W_UK, W_UV, o, lse=None, ws=None,
+                          stream=None):
+    T = q.shape[0]
+    if ws is None:
+        ws = workspace(mla_prefill_workspace_bytes(cfg, kv_len), q.device)
+    _check("mla_prefill_attention",
+           lib.mla_prefill_attention(ctypes.byref(cfg), _ptr(q), ctypes.byref(cache), seq, kv_len, T, _ptr(W_UK),
+                                     _ptr(W_UV), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+    return o
+
+
+def mla_head_output_workspace_bytes(cfg, N):
+    return int(lib.mla_head_output_workspace_bytes(ctypes.byref(cfg), N))
+
+
+def mla_head_output_project(cfg, o, W_O, out, ws=None, stream=None):
+    N = o.shape[0]
+    if ws is None:
+        ws = workspace(mla_head_output_workspace_bytes(cfg, N), o.device)
+    _check("mla_head_output_project",
+           lib.mla_head_output_project(ctypes.byref(cfg), _ptr(o), _ptr(W_O), _ptr(out), N, _ptr(ws), ws.numel(),
+                                       _stream(stream)))
     return out
 
 

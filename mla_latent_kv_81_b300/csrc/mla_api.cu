@@ -443,4 +443,73 @@ mla_status mla_selftest_wait_timeout(void* workspace, size_t workspace_bytes, ui
   return MLA_OK;
 }
 
+// ------------------------------------------------------------------ explicit form (prefill)
+size_t mla_project_workspace_bytes(const mla_config* cfg, int N) {
+  if (check_cfg(cfg) != MLA_OK || N < 0 || cfg->dtype != MLA_BF16) return 0;
+  if (N == 0) return kWsHeader;
+  return tc_project_supported(cfg, N) ? kWsHeader + tc_project_workspace_bytes(cfg, N, current_sm_count()) : 0;
+}
+
+mla_status mla_project_query(const mla_config* cfg, const void* x, const void* W_Q, const void* W_QR,
+                             const int32_t* q_pos, const mla_rope_table* rope, void* q_out, int N, void* workspace,
+                             size_t workspace_bytes, mla_stream_t stream) {
+  MLA_TRY(check_cfg(cfg));
+  if (N < 0) return MLA_ERR_INVALID_ARG;
+  if (N == 0) return MLA_OK;
+  if (!ok_ptr(x) || !ok_ptr(W_Q) || !ok_ptr(W_QR) || !ok_ptr(q_pos) || !ok_ptr(q_out)) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_rope(rope));
+  if (cfg->dtype != MLA_BF16 || !tc_project_supported(cfg, N)) return MLA_ERR_UNSUPPORTED;
+  MLA_TRY(check_workspace(workspace, workspace_bytes, mla_project_workspace_bytes(cfg, N)));
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, workspace, &ctx));
+  MLA_CUDA(tc_project_query(ctx, cfg, x, W_Q, W_QR, q_pos, *rope, q_out, N, ws_body(workspace)));
+  return MLA_OK;
+}
+
+size_t mla_prefill_workspace_bytes(const mla_config* cfg, int kv_len) {
+  if (check_cfg(cfg) != MLA_OK || kv_len <= 0 || cfg->dtype != MLA_BF16) return 0;
+  const size_t body = tc_prefill_workspace_bytes(cfg, kv_len);
+  return body ? kWsHeader + body : 0;
+}
+
+mla_status mla_prefill_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache, int seq,
+                                 int kv_len, int T, const void* W_UK, const void* W_UV, void* o, float* lse,
+                                 void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  MLA_TRY(check_cfg(cfg));
+  if (!ok_ptr(q) || !ok_ptr(W_UK) || !ok_ptr(W_UV) || !ok_ptr(o) || (lse && !aligned16(lse)))
+    return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_cache(cache));
+  if (seq < 0 || seq >= cache->batch || T < 1 || kv_len < T ||
+      (long long)kv_len > (long long)cache->max_blocks_per_seq * cfg->block_size)
+    return MLA_ERR_INVALID_ARG;
+  if (cfg->dtype != MLA_BF16 || !tc_prefill_supported(cfg)) return MLA_ERR_UNSUPPORTED;
+  MLA_TRY(check_workspace(workspace, workspace_bytes, mla_prefill_workspace_bytes(cfg, kv_len)));
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, workspace, &ctx));
+  MLA_CUDA(tc_prefill_attention(ctx, cfg, q, *cache, seq, kv_len, T, W_UK, W_UV, resolve_scale(cfg), o, lse,
+                                ws_body(workspace)));
+  return MLA_OK;
+}
+
+size_t mla_head_output_workspace_bytes(const mla_config* cfg, int N) {
+  if (check_cfg(cfg) != MLA_OK || N < 0 || cfg->dtype != MLA_BF16) return 0;
+  if (N == 0) return kWsHeader;
+  return tc_head_output_supported(cfg, N) ? kWsHeader + tc_head_output_workspace_bytes(cfg, N, current_sm_count())
+                                          : 0;
+}
+
+mla_status mla_head_output_project(const mla_config* cfg, const void* o, const void* W_O, void* out, int N,
+                                   void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  MLA_TRY(check_cfg(cfg));
+  if (N < 0) return MLA_ERR_INVALID_ARG;
+  if (N == 0) return MLA_OK;
+  if (!ok_ptr(o) || !ok_ptr(W_O) || !ok_ptr(out)) return MLA_ERR_INVALID_ARG;
+  if (cfg->dtype != MLA_BF16 || !tc_head_output_supported(cfg, N)) return MLA_ERR_UNSUPPORTED;
+  MLA_TRY(check_workspace(workspace, workspace_bytes, mla_head_output_workspace_bytes(cfg, N)));
+  Ctx ctx;
+  MLA_TRY(device_ctx(stream, workspace, &ctx));
+  MLA_CUDA(tc_head_output_project(ctx, cfg, o, W_O, out, N, ws_body(workspace)));
+  return MLA_OK;
+}
+
 }  // extern "C"

@@ -280,6 +280,39 @@ __global__ void absorb_reduce_kernel(const float* part, int splits, int N, int H
   }
 }
 
+// The explicit-form query from the same partials: q_out[n][h] = [q_nope^h (bf16) || RoPE(q_R^h) (bf16)].
+// One thread per 4 consecutive columns.
+__global__ void query_reduce_kernel(const float* part, int splits, int N, int H, int qk, int d_r, const int32_t* q_pos,
+                                    const float* rope, int rope_max, bf16* q_out, uint32_t* status) {
+  const int Mt = H * (qk + d_r);
+  const long long total4 = (long long)N * Mt / 4, stride = (long long)N * Mt;
+  for (long long e4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; e4 < total4;
+       e4 += (long long)gridDim.x * blockDim.x) {
+    const long long e = e4 * 4;
+    const int n = (int)(e / Mt), col = (int)(e % Mt);
+    const float4 v = sum_splits4(part, splits, stride, e);
+    __nv_bfloat162* dst;
+    float o0 = v.x, o1 = v.y, o2 = v.z, o3 = v.w;
+    if (col < H * qk) {
+      const int h = col / qk, i = col % qk;
+      dst = reinterpret_cast<__nv_bfloat162*>(q_out + ((long long)n * H + h) * (qk + d_r) + i);
+    } else {
+      const int c = col - H * qk, h = c / d_r, r = c % d_r;   // r even: two rotated pairs
+      const int p = q_pos[n];
+      if (p < 0 || p >= rope_max) {
+        flag_error(status, kFlagIndex);
+        continue;
+      }
+      const float* cs = rope + ((long long)p * (d_r / 2) + r / 2) * 2;
+      rope2(v.x, v.y, cs, o0, o1);
+      rope2(v.z, v.w, cs + 2, o2, o3);
+      dst = reinterpret_cast<__nv_bfloat162*>(q_out + ((long long)n * H + h) * (qk + d_r) + qk + r);
+    }
+    dst[0] = __floats2bfloat162_rn(o0, o1);
+    dst[1] = __floats2bfloat162_rn(o2, o3);
+  }
+}
+
 // Cache rows [c || RoPE(k_R)] from the k-split partials [splits][T][d_c + d_r] of the fused
 // W_DKV / W_KR GEMM, scattered into the paged pool, which stores each block transposed
 // ([d_c + d_r][block_size]).  Block (8-token group, 64-column group), warp w = token t0 + w: the partials
@@ -396,6 +429,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t d1, uin
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+}  // namespace
+
+// bf16 tensor map of any rank with the 128-byte swizzle (declared in mla_tc.cuh).
+bool encode_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                     const uint32_t* box) {
+  EncodeFn enc = encoder();
+  if (!enc || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; es[i] = 1; }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, st, b, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 
 struct GemmPlan {
   GemmArgs args;
@@ -631,6 +682,87 @@ cudaError_t tc_output_project(const Ctx& ctx, const mla_config* cfg, const void*
   const long long count = (long long)N * D;
   sum_to_bf16_kernel<<<launch_blocks(count / 4, 256, ctx.sm_count), 256, 0, ctx.stream>>>(
       l.po.args.partial, l.po.args.splits, count, static_cast<bf16*>(out));
+  count_launch();
+  return cudaGetLastError();
+}
+
+
+// ------------------------------------------------------------------ explicit form (prefill)
+// Query projection without absorption: q_out[n][h] = [W_Q^h x_n || RoPE(W_QR^h x_n, q_pos_n)].
+bool tc_project_supported(const mla_config* cfg, int N) {
+  return shapes_ok(cfg) && N > 0 && stack_ok(cfg->n_heads * cfg->qk_nope) && cfg->d_rope % 4 == 0 &&
+         cfg->qk_nope % 4 == 0;
+}
+
+size_t tc_project_workspace_bytes(const mla_config* cfg, int N, int sm_count) {
+  if (!tc_project_supported(cfg, N)) return 0;
+  const int H = cfg->n_heads;
+  return align256(partial_bytes(plan_stacked(H * cfg->qk_nope, H * cfg->d_rope, N, cfg->d_model, sm_count)));
+}
+
+cudaError_t tc_project_query(const Ctx& ctx, const mla_config* cfg, const void* x, const void* W_Q, const void* W_QR,
+                             const int32_t* q_pos, const mla_rope_table& rope, void* q_out, int N, void* workspace) {
+  const int D = cfg->d_model, H = cfg->n_heads, qk = cfg->qk_nope, d_r = cfg->d_rope;
+  GemmPlan pl = plan_stacked(H * qk, H * d_r, N, D, ctx.sm_count);
+  pl.args.partial = static_cast<float*>(workspace);
+  CUtensorMap aq, ar, bx;
+  if (!make_map(&aq, W_Q, D, (uint64_t)H * qk, 1, (uint64_t)D * 2, (uint64_t)D * 2 * H * qk, 128) ||
+      !make_map(&ar, W_QR, D, (uint64_t)H * d_r, 1, (uint64_t)D * 2, (uint64_t)D * 2 * H * d_r, 128) ||
+      !make_map(&bx, x, D, N, 1, (uint64_t)D * 2, (uint64_t)D * 2 * N, pl.args.n_tile))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_gemm(ctx, aq, ar, bx, pl);
+  if (e != cudaSuccess) return e;
+  const long long work = (long long)N * H * (qk + d_r) / 4;
+  query_reduce_kernel<<<launch_blocks(work, 256, ctx.sm_count), 256, 0, ctx.stream>>>(
+      pl.args.partial, pl.args.splits, N, H, qk, d_r, q_pos, rope.cos_sin, rope.max_pos, (bf16*)q_out, ctx.status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// Per-head keys and values rebuilt from token-major latent rows lat[L][d_c + d_rope] (the first d_c
+// elements): kv[t] = [W_UK^h c_t for every head h || W_UV^h c_t for every head h], bf16.  One GEMM
+// over the stacked up-projections, stored directly (K = d_c needs no k-split).
+cudaError_t tc_reconstruct_kv(const Ctx& ctx, const mla_config* cfg, const void* lat, int L, const void* W_UK,
+                              const void* W_UV, void* kv) {
+  const int H = cfg->n_heads, qk = cfg->qk_nope, v = cfg->v_head, d_c = cfg->d_c, row = cfg->d_c + cfg->d_rope;
+  GemmPlan pl = plan_gemm(H * qk + H * v, L, d_c, 1, false, true, ctx.sm_count);
+  pl.args.m_tiles1 = H * qk / 128;
+  pl.args.partial = nullptr;
+  pl.args.out = static_cast<bf16*>(kv);
+  pl.args.out_ld = (long long)H * (qk + v);
+  pl.args.out_g = 0;
+  CUtensorMap a1, a2, b;
+  if (!make_map(&a1, W_UK, d_c, (uint64_t)H * qk, 1, (uint64_t)d_c * 2, (uint64_t)d_c * 2 * H * qk, 128) ||
+      !make_map(&a2, W_UV, d_c, (uint64_t)H * v, 1, (uint64_t)d_c * 2, (uint64_t)d_c * 2 * H * v, 128) ||
+      !make_map(&b, lat, row, L, 1, (uint64_t)row * 2, (uint64_t)row * 2 * L, pl.args.n_tile))
+    return cudaErrorInvalidValue;
+  return launch_gemm(ctx, a1, a2, b, pl);
+}
+
+// out = W_O concat_h(o^h) for head outputs o[N][H][v_head] (bf16).
+bool tc_head_output_supported(const mla_config* cfg, int N) {
+  return shapes_ok(cfg) && N > 0 && cfg->d_model % 4 == 0;
+}
+
+size_t tc_head_output_workspace_bytes(const mla_config* cfg, int N, int sm_count) {
+  if (!tc_head_output_supported(cfg, N)) return 0;
+  return align256(partial_bytes(plan_gemm(cfg->d_model, N, cfg->n_heads * cfg->v_head, 1, false, false, sm_count)));
+}
+
+cudaError_t tc_head_output_project(const Ctx& ctx, const mla_config* cfg, const void* o, const void* W_O, void* out,
+                                   int N, void* workspace) {
+  const int D = cfg->d_model, Hv = cfg->n_heads * cfg->v_head;
+  GemmPlan po = plan_gemm(D, N, Hv, 1, false, false, ctx.sm_count);
+  po.args.partial = static_cast<float*>(workspace);
+  CUtensorMap awo, bo;
+  if (!make_map(&awo, W_O, (uint64_t)Hv, D, 1, (uint64_t)Hv * 2, (uint64_t)Hv * 2 * D, 128) ||
+      !make_map(&bo, o, (uint64_t)Hv, N, 1, (uint64_t)Hv * 2, (uint64_t)Hv * 2 * N, po.args.n_tile))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_gemm(ctx, awo, awo, bo, po);
+  if (e != cudaSuccess) return e;
+  const long long count = (long long)N * D;
+  sum_to_bf16_kernel<<<launch_blocks(count / 4, 256, ctx.sm_count), 256, 0, ctx.stream>>>(
+      po.args.partial, po.args.splits, count, static_cast<bf16*>(out));
   count_launch();
   return cudaGetLastError();
 }

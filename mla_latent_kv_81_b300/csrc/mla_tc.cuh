@@ -1,6 +1,8 @@
 // Tensor-core (tcgen05 / TMEM / TMA) kernels for the bf16 DeepSeek-V2-shaped layer.
 #pragma once
 
+#include <cuda.h>
+
 #include "mla_common.cuh"
 
 namespace mla {
@@ -27,6 +29,29 @@ bool tc_output_supported(const mla_config* cfg, int N);
 size_t tc_output_workspace_bytes(const mla_config* cfg, int N, int sm_count);
 cudaError_t tc_output_project(const Ctx& ctx, const mla_config* cfg, const void* o_lat, const void* W_UV,
                               const void* W_O, void* out, int N, void* workspace);
+
+// Explicit form (prefill): query projection without absorption, per-head K / V rebuilt from the latent,
+// causal attention per head, and the output projection of per-head outputs.
+bool tc_project_supported(const mla_config* cfg, int N);
+size_t tc_project_workspace_bytes(const mla_config* cfg, int N, int sm_count);
+cudaError_t tc_project_query(const Ctx& ctx, const mla_config* cfg, const void* x, const void* W_Q, const void* W_QR,
+                             const int32_t* q_pos, const mla_rope_table& rope, void* q_out, int N, void* workspace);
+cudaError_t tc_reconstruct_kv(const Ctx& ctx, const mla_config* cfg, const void* lat, int L, const void* W_UK,
+                              const void* W_UV, void* kv);
+bool tc_prefill_supported(const mla_config* cfg);
+size_t tc_prefill_workspace_bytes(const mla_config* cfg, int kv_len);
+cudaError_t tc_prefill_attention(const Ctx& ctx, const mla_config* cfg, const void* q, const mla_paged_cache& cache,
+                                 int seq, int kv_len, int T, const void* W_UK, const void* W_UV, float scale, void* o,
+                                 float* lse, void* workspace);
+bool tc_head_output_supported(const mla_config* cfg, int N);
+size_t tc_head_output_workspace_bytes(const mla_config* cfg, int N, int sm_count);
+cudaError_t tc_head_output_project(const Ctx& ctx, const mla_config* cfg, const void* o, const void* W_O, void* out,
+                                   int N, void* workspace);
+
+// bf16 tensor map of rank 1..5 with the 128-byte swizzle: dims[0] innermost, strides[i] the byte
+// stride of dimension i + 1, box the copied extent per dimension.
+bool encode_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                     const uint32_t* box);
 
 // Self-check of the bounded waits: one thread waits on an mbarrier nothing completes, gives up after
 // limit_cycles and sets the timeout flag in ctx.status.

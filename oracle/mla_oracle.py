@@ -191,6 +191,41 @@ def attend_explicit(q_nope, q_rope, c, k_r, W_UK, W_UV, kv_len: int, scale: floa
     return out
 
 
+def attend_explicit_at(q_nope, q_rope, pos, c, k_r, W_UK, W_UV, scale: float, store=None):
+    """Explicit attention for queries at given positions of one sequence: query j
+    sees the tokens at positions 0..pos[j] (a prompt at prefill, every prompt
+    token a query: [TM point 4], keys and values recomputed from the latent;
+    visibility is reading c5 with the query's own row already cached).
+
+    The same definition as attend_explicit -- K and V rebuilt per head from c,
+    score = scale (q_nope . k + q_R . k_R), softmax, weighted sum of V -- with
+    each head's K and V rebuilt once for all the queries.
+    q_nope [n, H, qk_nope], q_rope [n, H, d_rope], pos int [n], c [L, d_c],
+    k_r [L, d_rope] with L > max(pos).
+    store: applied to each head's rebuilt K and V before use (a bf16 pipeline
+    stores them in bf16: pass round_bf16, reading c20); default keeps them exact.
+    Returns o [n, H, v_head] and lse [n, H] (natural log of the softmax
+    normaliser of the scaled scores).
+    """
+    q_nope, q_rope, c, k_r = _a(q_nope), _a(q_rope), _a(c), _a(k_r)
+    pos = np.asarray(pos, dtype=np.int64)
+    n, H, _ = q_nope.shape
+    v_head = _a(W_UV).shape[1]
+    top = int(pos.max()) + 1
+    o = np.zeros((n, H, v_head), dtype=f64)
+    lse = np.zeros((n, H), dtype=f64)
+    for h in range(H):
+        K_h, V_h = reconstruct_kv(c[:top], W_UK, W_UV, h)
+        if store is not None:
+            K_h, V_h = store(K_h), store(V_h)
+        for j in range(n):
+            vis = int(pos[j]) + 1
+            s = scale * (K_h[:vis] @ q_nope[j, h] + k_r[:vis] @ q_rope[j, h])
+            p, lse[j, h] = _softmax_weights(s)
+            o[j, h] = p @ V_h[:vis]
+    return o, lse
+
+
 def output_project(o, W_O):
     """out = W_O concat_h(o^h).  [KJ §Why it is not just extra work] output projection."""
     o = _a(o)

@@ -40,6 +40,24 @@ def assert_close(got, ref, dtype: str, what: str = ""):
     return err
 
 
+def assert_close_rows(got, ref, what: str = "", tol: float = BF16_TOL):
+    """The bf16 measure of rel_err applied to each query token on its own (reading c20): the outputs of
+    one prompt's queries average 1..L tokens, so their magnitudes differ by up to sqrt(L) and one
+    global RMS would hold the long rows to a loose bound and the short rows to a tight one."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    n = ref.shape[0]
+    g, r = got.reshape(n, -1), ref.reshape(n, -1)
+    rms = np.sqrt(np.mean(r * r, axis=1))
+    excess = np.maximum(np.abs(g - r) - bf16_half_ulp(r), 0.0)
+    err = excess.max(axis=1) / rms
+    worst = int(np.argmax(err))
+    assert err[worst] <= tol, f"{what}: query row {worst}: relative error {err[worst]:.3e} > {tol:g}"
+    return float(err[worst])
+
+
 def logical_cache(p: I.Problem, b: int):
     """Oracle-side cache rows of sequence b (float64): drawn rows or rows projected from x_ctx,
     then the appended query tokens projected from x_q."""

@@ -171,6 +171,33 @@ def check_sdpa(seed, d_model, H, qk_nope, d_rope, v_head, d_c, L, n_q, tol=1e-12
     assert err <= tol, err
 
 
+def check_prefill_rows(seed, d_model, H, qk_nope, d_rope, v_head, d_c, L, pos, tol=1e-12):
+    """attend_explicit_at against torch's scaled_dot_product_attention (CPU, float64) with the
+    prompt's causal mask over the rebuilt K and V; its lse against the absorbed form's (the pages'
+    invariant: scores are the same either way)."""
+    import torch
+    pos = np.asarray(pos)
+    n = len(pos)
+    W, x_ctx, x_q = small_problem(seed, d_model, H, qk_nope, d_rope, v_head, d_c, L, n, sharp=2.0)
+    c, k_r = O.compress(x_ctx, W["W_DKV"], W["W_KR"], np.arange(L))
+    q_nope, q_rope = O.project_query(x_q, W["W_Q"], W["W_QR"], pos, H)
+    scale = O.softmax_scale(qk_nope, d_rope)
+    got, lse = O.attend_explicit_at(q_nope, q_rope, pos, c, k_r, W["W_UK"], W["W_UV"], scale)
+    K = np.stack([np.concatenate([O.reconstruct_kv(c, W["W_UK"], W["W_UV"], h)[0], k_r], axis=1) for h in range(H)])
+    V = np.stack([O.reconstruct_kv(c, W["W_UK"], W["W_UV"], h)[1] for h in range(H)])
+    Q = np.concatenate([q_nope, q_rope], axis=2).transpose(1, 0, 2)
+    mask = np.arange(L)[None, :] <= pos[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+        attn_mask=torch.from_numpy(mask), scale=scale)[0].numpy().transpose(1, 0, 2)
+    err = np.max(np.abs(got - ref)) / np.max(np.abs(ref))
+    assert err <= tol, err
+    q_abs = O.absorb_query(q_nope, W["W_UK"])
+    for j in range(n):
+        _, lse_abs = O.attend_latent(q_abs[j:j + 1], q_rope[j:j + 1], c, k_r, int(pos[j]) + 1, scale)
+        assert np.max(np.abs(lse[j] - lse_abs[0])) <= 1e-10
+
+
 def check_rope_properties(d_rope=16, base=10000.0):
     rng = np.random.default_rng(7)
     v = rng.standard_normal((5, d_rope))

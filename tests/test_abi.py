@@ -158,3 +158,32 @@ def test_bad_arguments_fail_before_any_launch():
     odd.d_rope = 15
     assert lib.mla_output_project(byref(odd), _fake(1), _fake(2), _fake(3), _fake(4), 4, _fake(6), 1 << 30,
                                   None) == 2
+
+
+def test_prefill_entry_points_check_arguments_on_the_host():
+    """The explicit-form calls: bf16 tensor-core shapes only, 1 <= T <= kv_len <= the sequence's
+    blocks, seq inside the batch; all checked before any launch."""
+    lib, byref = M.lib, ctypes.byref
+    INV, UNS = 1, 2
+    cfg = M.make_config(I.DSV2, "bf16")
+    f32 = M.make_config(I.TINY, "f32")
+    assert M.mla_prefill_workspace_bytes(cfg, 4096) >= 256 + 4096 * (576 + 2 * 128 * 128) * 2
+    assert M.mla_prefill_workspace_bytes(cfg, 0) == 0
+    assert M.mla_prefill_workspace_bytes(f32, 10) == 0
+    assert M.mla_project_workspace_bytes(f32, 4) == 0
+    assert M.mla_head_output_workspace_bytes(f32, 4) == 0
+    assert M.mla_project_workspace_bytes(cfg, 0) == 256
+    cache = M.mla_paged_cache(0x2000, 40, 0x3000, 4, 2)     # 4 blocks of 64 per sequence, 2 sequences
+    args = lambda seq, kv, T: (byref(cfg), _fake(1), byref(cache), seq, kv, T, _fake(2), _fake(3), _fake(4), None,
+                               _fake(5), 1 << 40, None)
+    assert lib.mla_prefill_attention(*args(0, 100, 101)) == INV    # T > kv_len
+    assert lib.mla_prefill_attention(*args(0, 100, 0)) == INV      # T = 0
+    assert lib.mla_prefill_attention(*args(2, 100, 10)) == INV     # seq outside the batch
+    assert lib.mla_prefill_attention(*args(0, 257, 10)) == INV     # more tokens than the sequence's blocks
+    assert lib.mla_prefill_attention(byref(f32), _fake(1), byref(cache), 0, 8, 4, _fake(2), _fake(3), _fake(4),
+                                     None, _fake(5), 1 << 40, None) == UNS
+    rope = M.mla_rope_table(0x1000, 16)
+    assert lib.mla_project_query(byref(f32), _fake(1), _fake(2), _fake(3), _fake(4), byref(rope), _fake(5), 4,
+                                 _fake(6), 1 << 30, None) == UNS
+    assert lib.mla_head_output_project(byref(f32), _fake(1), _fake(2), _fake(3), 4, _fake(6), 1 << 30, None) == UNS
+    assert lib.mla_head_output_project(byref(cfg), None, _fake(2), _fake(3), 4, _fake(6), 1 << 30, None) == INV

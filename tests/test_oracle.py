@@ -38,6 +38,16 @@ def test_sdpa_library(shape):
     pins.check_sdpa(seed=3, **shape)
 
 
+@pytest.mark.parametrize("shape", [
+    # a whole prompt of 9 tokens, every token a query
+    dict(d_model=40, H=3, qk_nope=7, d_rope=4, v_head=9, d_c=11, L=9, pos=list(range(9))),
+    # scattered positions of a longer prompt, out of order, one of them the first token
+    dict(d_model=64, H=4, qk_nope=16, d_rope=8, v_head=12, d_c=20, L=50, pos=[49, 0, 17, 31, 32, 8]),
+])
+def test_prefill_rows_against_sdpa(shape):
+    pins.check_prefill_rows(seed=6, **shape)
+
+
 def test_rope_properties():
     pins.check_rope_properties(16)
     pins.check_rope_properties(64)
