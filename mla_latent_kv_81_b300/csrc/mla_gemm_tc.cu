@@ -46,6 +46,8 @@ struct GemmArgs {
   float* partial;                     // [splits][G][N][M] fp32, or null
   bf16* out;                          // direct bf16 output when partial == null
   long long out_ld, out_g;            // out[g * out_g + n * out_ld + m]
+  long long out_mc;                   // > 0: out stored chunk-major, out[(m / 64) * out_mc + n * 64 + m % 64]
+  int b_kchunk;                       // B stored chunk-major [K / 64][N][64] (one contiguous box per k-block)
   uint32_t* status;
 };
 
@@ -130,7 +132,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
           } else {
             tma_load_3d(sa, am, &ctrl->full[st], ka, ma, g);
           }
-          tma_load_3d(sb, &b_map, &ctrl->full[st], kb * 64, nt * a.n_tile, g);
+          if (a.b_kchunk)
+            tma_load_3d(sb, &b_map, &ctrl->full[st], 0, nt * a.n_tile, kb);
+          else
+            tma_load_3d(sb, &b_map, &ctrl->full[st], kb * 64, nt * a.n_tile, g);
           if (++st == a.stages) { st = 0; ph ^= 1; }
         }
       }
@@ -197,11 +202,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
               if (n < a.N) dst[(long long)n * a.M] = __uint_as_float(r[i]);
             }
           } else {
-            bf16* dst = a.out + (long long)g * a.out_g + m;
+            const long long ld = a.out_mc ? 64 : a.out_ld;
+            bf16* dst = a.out + (a.out_mc ? (long long)(m >> 6) * a.out_mc + (m & 63) : (long long)g * a.out_g + m);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int n = n0 + c + i;
-              if (n < a.N) dst[(long long)n * a.out_ld] = __float2bfloat16_rn(__uint_as_float(r[i]));
+              if (n < a.N) dst[(long long)n * ld] = __float2bfloat16_rn(__uint_as_float(r[i]));
             }
           }
         }
@@ -719,22 +725,26 @@ cudaError_t tc_project_query(const Ctx& ctx, const mla_config* cfg, const void* 
   return cudaGetLastError();
 }
 
-// Per-head keys and values rebuilt from token-major latent rows lat[L][d_c + d_rope] (the first d_c
-// elements): kv[t] = [W_UK^h c_t for every head h || W_UV^h c_t for every head h], bf16.  One GEMM
-// over the stacked up-projections, stored directly (K = d_c needs no k-split).
+// Per-head keys and values rebuilt from the latent rows, stored chunk-major lat[(d_c + d_rope) / 64][L][64]
+// (the first d_c / 64 chunks are read): row m of the stacked up-projections [W_UK (all heads); W_UV (all
+// heads)] times c_t goes to kv[m / 64][t][m % 64], bf16.  Both layouts make every TMA box one contiguous
+// run.  One GEMM, stored directly (K = d_c needs no k-split).
 cudaError_t tc_reconstruct_kv(const Ctx& ctx, const mla_config* cfg, const void* lat, int L, const void* W_UK,
                               const void* W_UV, void* kv) {
   const int H = cfg->n_heads, qk = cfg->qk_nope, v = cfg->v_head, d_c = cfg->d_c, row = cfg->d_c + cfg->d_rope;
+  if (qk % 64 || v % 64 || row % 64) return cudaErrorInvalidValue;
   GemmPlan pl = plan_gemm(H * qk + H * v, L, d_c, 1, false, true, ctx.sm_count);
   pl.args.m_tiles1 = H * qk / 128;
   pl.args.partial = nullptr;
   pl.args.out = static_cast<bf16*>(kv);
-  pl.args.out_ld = (long long)H * (qk + v);
+  pl.args.out_ld = 64;
   pl.args.out_g = 0;
+  pl.args.out_mc = (long long)L * 64;
+  pl.args.b_kchunk = 1;
   CUtensorMap a1, a2, b;
   if (!make_map(&a1, W_UK, d_c, (uint64_t)H * qk, 1, (uint64_t)d_c * 2, (uint64_t)d_c * 2 * H * qk, 128) ||
       !make_map(&a2, W_UV, d_c, (uint64_t)H * v, 1, (uint64_t)d_c * 2, (uint64_t)d_c * 2 * H * v, 128) ||
-      !make_map(&b, lat, row, L, 1, (uint64_t)row * 2, (uint64_t)row * 2 * L, pl.args.n_tile))
+      !make_map(&b, lat, 64, L, row / 64, 128, (uint64_t)L * 128, pl.args.n_tile))
     return cudaErrorInvalidValue;
   return launch_gemm(ctx, a1, a2, b, pl);
 }

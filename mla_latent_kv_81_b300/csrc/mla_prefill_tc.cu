@@ -8,22 +8,31 @@
 // this form costs 2 (qk_nope + d_rope + v_head) FLOP per (query, key, head), against
 // 2 (d_c + d_rope + d_c) for the absorbed form, so the keys and values are rebuilt once:
 //   1. gather_latent_kernel: the sequence's rows, stored element-major per cache block, into one
-//      token-major buffer lat[L][d_c + d_rope];
-//   2. tc_reconstruct_kv (projection GEMM): kv[t] = [W_UK^h c_t for all h || W_UV^h c_t for all h];
+//      chunk-major buffer lat[(d_c + d_rope) / 64][L][64];
+//   2. tc_reconstruct_kv (projection GEMM): per-head keys W_UK^h c_t and values W_UV^h c_t, chunk-major
+//      kv[4H][L][64] (64-element chunk 2h + c of head h's key, 2H + 2h + c of its value);
+//   Every TMA box of the GEMM and of the attention kernel over these buffers is one contiguous run
+//   (rows of 128 B 1 KB or more apart had held a box to a fraction of the per-SM copy rate).
 //   3. prefill_attn_kernel: per (head, 128-query tile) unit, scores S = Q K^T over 128-key tiles with
 //      K = [W_UK^h c_t || k_R,t] (the positional key shared by all heads, taken from lat; its score
 //      added to the content score, "Multi-head Latent Attention (MLA)" Implementation Logic step 5,
 //      reading c2), causal online softmax, O += P V, O = softmax . V^h.
 //
 // Kernel layout (one CTA per SM, persistent over units, 256 threads):
-//   warp 0: TMA producer; warp 1: MMA issuer (one thread); warp 2: TMEM allocation;
-//   warps 4-7: softmax, one thread per query row (TMEM lane), then the epilogue.
+//   warp 0: TMA producer of the key ring; warp 3: TMA producer of the value ring; warp 1: MMA issuer
+//   (one thread); warp 2: TMEM allocation;
+//   warps 4-11: softmax and epilogue, two threads per query row (TMEM lane): warps 4-7 take key columns
+//   0-63 of S and value columns 0-63 of O, warps 8-11 columns 64-127; the two halves of a row exchange
+//   their maxima (and, at the end of a unit, their row sums) through shared memory and a bounded
+//   mbarrier.
 //   TMEM: S double-buffered in columns [0, 256), O in [256, 384), the query in [384, 480)
-//   (copied from shared memory with tcgen05.cp, the A operand of the score MMAs).
-//   Shared memory: a ring of 48 KB slots for the query (3 chunks of 64 elements) and the key tiles
-//   (K_nope: 2 chunks, k_R: 1 chunk, each [128 tokens][128 B] with the 128-byte swizzle); a ring of
-//   32 KB value slots ([2 chunks of 64 dims][128 tokens][128 B], an MN-major B operand); one 32 KB
-//   buffer of P (bf16, K-major A operand of the P V MMAs).
+//   (copied from shared memory with tcgen05.cp, the A operand of the score MMAs).  P (bf16) is written
+//   over the first 64 columns of its own S buffer and read from there as the A operand of P V.
+//   Shared memory: a ring of nine 16 KB chunk slots for the query chunks and the key tiles (K_nope: 2
+//   chunks, k_R: 1 chunk, each [128 tokens][128 B] with the 128-byte swizzle), three key tiles deep;
+//   a ring of two 32 KB value slots ([2 chunks of 64 dims][128 tokens][128 B], an MN-major B operand).
+//   The loads run up to three tiles ahead: the kernel's pace is otherwise set by the latency of the
+//   copies (bytes in flight per SM), not by the tensor cores or the softmax.
 #include <math.h>
 
 #include "mla_sm100.cuh"
@@ -38,14 +47,13 @@ constexpr int kQW = kQK + kDR;            // query row [q_nope || q_R]
 constexpr int kFT = 128;                  // queries per tile, keys per tile
 constexpr int kFBlk = 64;                 // cache block size the kernel is built for
 constexpr int kChunk = kFT * 128;         // [128 rows][64 bf16] = 16 KB
-constexpr int kSSlot = 3 * kChunk;        // query, or K_nope (2 chunks) + k_R (1 chunk)
-constexpr int kVSlot = 2 * kChunk;        // V (2 chunks of 64 dims)
-constexpr int kSRing = 2, kVRing = 2;
-constexpr int kFThreads = 256;
-constexpr int kOffSRing = 1024;
-constexpr int kOffVRing = kOffSRing + kSRing * kSSlot;
-constexpr int kOffP = kOffVRing + kVRing * kVSlot;
-constexpr int kFSmem = kOffP + 2 * kChunk + 1024;   // + alignment slack of the dynamic base
+constexpr int kKSlots = 9;                // K ring: 16 KB chunk slots (query chunks, then 3 per key tile)
+constexpr int kVSlot = 2 * kChunk;        // V ring slot: the tile's two 64-dim chunks, adjacent
+constexpr int kVRing = 2;
+constexpr int kFThreads = 384;
+constexpr int kOffKRing = 4096;
+constexpr int kOffVRing = kOffKRing + kKSlots * kChunk;
+constexpr int kFSmem = kOffVRing + kVRing * kVSlot + 1024;   // + alignment slack of the dynamic base
 constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
 constexpr float kFLazy = 8.f;                        // the running max moves when it grows by > 2^8
 
@@ -53,12 +61,14 @@ static_assert(kFSmem <= 232448, "shared memory of one CTA");
 static_assert(kQW == 3 * 64 && kQK == 2 * 64 && kVH == 2 * 64, "64-element chunks");
 
 struct FCtrl {
-  uint64_t k_full[kSRing], k_empty[kSRing], v_full[kVRing], v_empty[kVRing];
-  uint64_t s_full[2], s_empty[2], p_full, pv_done, o_free;
+  uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[kVRing], v_empty[kVRing];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_free;   // one s_full / p_full / pv_done per S buffer
+  uint64_t xch[2];                 // exchanges between the two halves of each row (alternating)
   uint32_t tmem_base;
   int abort_flag;
+  float xval[2][2][128];           // [exchange parity][half][row]: half-row maxima, or partial row sums
 };
-static_assert(sizeof(FCtrl) <= kOffSRing, "control block");
+static_assert(sizeof(FCtrl) <= kOffKRing, "control block");
 
 struct FParams {
   int T, L, q0;       // queries, keys (cached prompt rows), position of query 0 (= L - T)
@@ -89,10 +99,10 @@ __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
 }
 
 // ------------------------------------------------------------------ gather
-// lat[t][e] = element e of the token at position t of sequence `seq`, for t < L.  Block (64-token
-// cache block, 64-element group): the block's element rows (64 tokens, contiguous) are read, transposed
-// through shared memory and written token-major.  Out-of-range block-table entries flag an index
-// error and give zero rows.
+// lat[e / 64][t][e % 64] = element e of the token at position t of sequence `seq`, for t < L.  Block
+// (64-token cache block, 64-element chunk): the block's element rows (64 tokens, contiguous) are read,
+// transposed through shared memory and written as 64 rows of 128 B (one contiguous 8 KB run).
+// Out-of-range block-table entries flag an index error and give zero rows.
 __global__ void __launch_bounds__(256) gather_latent_kernel(const bf16* pool, const int32_t* table, int max_blocks,
                                                             int num_blocks, int seq, int L, bf16* lat,
                                                             uint32_t* status) {
@@ -113,13 +123,13 @@ __global__ void __launch_bounds__(256) gather_latent_kernel(const bf16* pool, co
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
     const int t = i >> 6, e = i & 63;
     const int pos = bt * kFBlk + t;
-    if (pos < L) dst[(long long)pos * kRowW + e0 + e] = tile[e][t];
+    if (pos < L) dst[((long long)blockIdx.y * L + pos) * 64 + e] = tile[e][t];
   }
 }
 
 // ------------------------------------------------------------------ attention
-// mapq: q [T][H][192] as {192, H, T}; mapkv: kv [L][2H][128] as {128, 2H, L} (heads H.. are V);
-// mapr: lat [L][576] as {576, L}.  Boxes of 64 elements x 128 rows, out-of-range rows read as zero.
+// mapq: q [T][H][192] as {192, H, T}, box {64, 1, 128}; mapkv: kv [4H][L][64] as {64, L, 4H} and mapr:
+// lat [9][L][64] as {64, L, 9}, boxes {64, 128, 1}.  Out-of-range rows read as zero.
 __global__ void __launch_bounds__(kFThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap mapq, const __grid_constant__ CUtensorMap mapkv,
                         const __grid_constant__ CUtensorMap mapr, FParams p) {
@@ -130,12 +140,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
   volatile int* abort_flag = &ctrl->abort_flag;
 
   if (tid == 0) {
-    for (int i = 0; i < kSRing; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
+    for (int i = 0; i < kKSlots; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
     for (int i = 0; i < kVRing; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&ctrl->s_full[i], 1); mbar_init(&ctrl->s_empty[i], 128); }
-    mbar_init(&ctrl->p_full, 128);
-    mbar_init(&ctrl->pv_done, 1);
-    mbar_init(&ctrl->o_free, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctrl->s_full[i], 1);
+      mbar_init(&ctrl->p_full[i], 256);
+      mbar_init(&ctrl->pv_done[i], 1);
+      mbar_init(&ctrl->xch[i], 256);
+    }
+    mbar_init(&ctrl->o_free, 256);
     ctrl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -156,52 +169,57 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // producer, in the order the MMA thread consumes: the query, K(0), then K(j), V(j-1) for
-      // j = 1..n-1, then V(n-1)
-      int kr = 0, vr = 0;
-      uint32_t kph = 0, vph = 0;
+      // key producer, in the order the MMA thread consumes the key ring: the query's 3 chunks, then the
+      // 3 chunks of each key tile.  One 16 KB chunk per slot.
+      int kr = 0;
+      uint32_t kph = 0;
+      auto load_chunk = [&](const CUtensorMap* map, int c0, int c1, int c2) -> bool {
+        if (!mbar_wait_cta(&ctrl->k_empty[kr], kph ^ 1, p.status, abort_flag)) return false;
+        mbar_arrive_expect_tx(&ctrl->k_full[kr], kChunk);
+        tma_load_3d(smem + kOffKRing + kr * kChunk, map, &ctrl->k_full[kr], c0, c1, c2);
+        if (++kr == kKSlots) { kr = 0; kph ^= 1; }
+        return true;
+      };
       for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         int h, qt, n, p0;
         unit_of(p, u, h, qt, n, p0);
-        if (!mbar_wait_cta(&ctrl->k_empty[kr], kph ^ 1, p.status, abort_flag)) goto done;
-        {
-          uint8_t* dst = smem + kOffSRing + kr * kSSlot;
-          mbar_arrive_expect_tx(&ctrl->k_full[kr], kSSlot);
-#pragma unroll
-          for (int c = 0; c < 3; ++c) tma_load_3d(dst + c * kChunk, &mapq, &ctrl->k_full[kr], c * 64, h, qt * kFT);
-        }
-        if (++kr == kSRing) { kr = 0; kph ^= 1; }
-        for (int j = 0; j <= n; ++j) {
-          if (j < n) {
-            if (!mbar_wait_cta(&ctrl->k_empty[kr], kph ^ 1, p.status, abort_flag)) goto done;
-            uint8_t* dst = smem + kOffSRing + kr * kSSlot;
-            mbar_arrive_expect_tx(&ctrl->k_full[kr], kSSlot);
-            tma_load_3d(dst, &mapkv, &ctrl->k_full[kr], 0, h, j * kFT);
-            tma_load_3d(dst + kChunk, &mapkv, &ctrl->k_full[kr], 64, h, j * kFT);
-            tma_load_2d(dst + 2 * kChunk, &mapr, &ctrl->k_full[kr], kDC, j * kFT);
-            if (++kr == kSRing) { kr = 0; kph ^= 1; }
-          }
-          if (j >= 1) {
-            if (!mbar_wait_cta(&ctrl->v_empty[vr], vph ^ 1, p.status, abort_flag)) goto done;
-            uint8_t* dst = smem + kOffVRing + vr * kVSlot;
-            mbar_arrive_expect_tx(&ctrl->v_full[vr], kVSlot);
-            tma_load_3d(dst, &mapkv, &ctrl->v_full[vr], 0, p.H + h, (j - 1) * kFT);
-            tma_load_3d(dst + kChunk, &mapkv, &ctrl->v_full[vr], 64, p.H + h, (j - 1) * kFT);
-            if (++vr == kVRing) { vr = 0; vph ^= 1; }
-          }
+        for (int c = 0; c < 3; ++c)
+          if (!load_chunk(&mapq, c * 64, h, qt * kFT)) goto done;
+        for (int j = 0; j < n; ++j)
+          if (!load_chunk(&mapkv, 0, j * kFT, 2 * h) || !load_chunk(&mapkv, 0, j * kFT, 2 * h + 1) ||
+              !load_chunk(&mapr, 0, j * kFT, kDC / 64))
+            goto done;
+      }
+    }
+  } else if (warp == 3) {
+    if (lane == 0) {
+      // value producer: one tile of V per slot.  Its own thread, so that a full value ring never holds
+      // back the key loads (the copies take microseconds under load: the key ring must run ahead)
+      int vr = 0;
+      uint32_t vph = 0;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        int h, qt, n, p0;
+        unit_of(p, u, h, qt, n, p0);
+        for (int j = 0; j < n; ++j) {
+          if (!mbar_wait_cta(&ctrl->v_empty[vr], vph ^ 1, p.status, abort_flag)) goto done;
+          uint8_t* dst = smem + kOffVRing + vr * kVSlot;
+          mbar_arrive_expect_tx(&ctrl->v_full[vr], kVSlot);
+          tma_load_3d(dst, &mapkv, &ctrl->v_full[vr], 0, j * kFT, 2 * p.H + 2 * h);
+          tma_load_3d(dst + kChunk, &mapkv, &ctrl->v_full[vr], 0, j * kFT, 2 * p.H + 2 * h + 1);
+          if (++vr == kVRing) { vr = 0; vph ^= 1; }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // S (128 queries x 128 keys) = Q K^T: A = the query in TMEM (8 columns per 16-element K-step),
-      // B = the key slot (K-major, 32 B per K-step).  O (128 x 128) += P V: A = P (K-major, two
-      // 64-key chunks), B = the value slot (MN-major: 64-dim chunks kChunk apart, 2048 B per 16 keys).
+      // B = a key chunk slot (K-major, 32 B per K-step).  O (128 x 128) += P V: A = P, written by the
+      // softmax over the first 64 columns of its own S buffer (bf16 pairs, 8 columns per 16 keys),
+      // B = the value slot (MN-major: 64-dim chunks kChunk apart, 2048 B per 16 keys).
       const uint32_t idesc_s = idesc_bf16(128, kFT, false, false);
       const uint32_t idesc_pv = idesc_bf16(128, kVH, false, true);
-      const uint64_t kdesc0 = desc_sw128(sbase + kOffSRing, 16, 1024);
+      const uint64_t kdesc0 = desc_sw128(sbase + kOffKRing, 16, 1024);
       const uint64_t vdesc0 = desc_sw128(sbase + kOffVRing, kChunk, 1024);
-      const uint64_t pdesc0 = desc_sw128(sbase + kOffP, 16, 1024);
       const uint32_t tq = tmem + kColQ, to = tmem + kColO;
       int kr = 0, vr = 0, g = 0, nu = 0;
       uint32_t kph = 0, vph = 0;
@@ -210,50 +228,55 @@ __global__ void __launch_bounds__(kFThreads, 1)
         unit_of(p, u, h, qt, n, p0);
         // the unit's query into TMEM: this thread's tcgen05 operations run in issue order, so the copies
         // land only after the previous unit's score MMAs have read the old query
-        if (!mbar_wait_cta(&ctrl->k_full[kr], kph, p.status, abort_flag)) goto done;
-        tc_fence_after();
-        {
-          const uint64_t qd = kdesc0 + (uint64_t)(kr * (kSSlot >> 4));
+        for (int c = 0; c < 3; ++c) {
+          if (!mbar_wait_cta(&ctrl->k_full[kr], kph, p.status, abort_flag)) goto done;
+          tc_fence_after();
+          const uint64_t qd = kdesc0 + (uint64_t)(kr * (kChunk >> 4));
 #pragma unroll
-          for (int c = 0; c < 3; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tmem_cp_128x256b(tq + c * 32 + k * 8, qd + (uint64_t)(c * (kChunk >> 4) + k * 2));
+          for (int k = 0; k < 4; ++k) tmem_cp_128x256b(tq + c * 32 + k * 8, qd + (uint64_t)(k * 2));
+          mma_commit(&ctrl->k_empty[kr]);
+          if (++kr == kKSlots) { kr = 0; kph ^= 1; }
         }
-        mma_commit(&ctrl->k_empty[kr]);
-        if (++kr == kSRing) { kr = 0; kph ^= 1; }
         for (int j = 0; j <= n; ++j) {
           if (j < n) {
             const int gs = g + j, buf = gs & 1;
-            if (!mbar_wait_cta(&ctrl->s_empty[buf], ((gs >> 1) & 1) ^ 1, p.status, abort_flag)) goto done;
-            if (!mbar_wait_cta(&ctrl->k_full[kr], kph, p.status, abort_flag)) goto done;
-            tc_fence_after();
-            const uint64_t kd = kdesc0 + (uint64_t)(kr * (kSSlot >> 4));
+            // S buffer buf last held P(gs - 2), read by P V(gs - 2): that MMA was issued by this thread
+            // before, and tcgen05 operations of one thread run in issue order, so S(gs) may be queued now
             const uint32_t d = tmem + kColS + buf * kFT;
 #pragma unroll
-            for (int c = 0; c < 3; ++c)
+            for (int c = 0; c < 3; ++c) {
+              if (!mbar_wait_cta(&ctrl->k_full[kr], kph, p.status, abort_flag)) goto done;
+              tc_fence_after();
+              const uint64_t kd = kdesc0 + (uint64_t)(kr * (kChunk >> 4));
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_ts(d, tq + c * 32 + k * 8, kd + (uint64_t)(c * (kChunk >> 4) + k * 2), idesc_s,
-                       (c | k) ? 1u : 0u);
-            mma_commit(&ctrl->k_empty[kr]);
+                mma_ts(d, tq + c * 32 + k * 8, kd + (uint64_t)(k * 2), idesc_s, (c | k) ? 1u : 0u);
+              mma_commit(&ctrl->k_empty[kr]);
+              if (++kr == kKSlots) { kr = 0; kph ^= 1; }
+            }
             mma_commit(&ctrl->s_full[buf]);
-            if (++kr == kSRing) { kr = 0; kph ^= 1; }
+            // P V(gs - 2) done before anything later: every wait on a pv_done barrier (this one, the
+            // softmax's before a rescale, the epilogue's) then finds its barrier at most one phase short
+            // of the completion it names (the barriers are per S buffer because at a unit's first tile
+            // P V(gs - 1) has already been issued)
+            if (gs >= 2 && !mbar_wait_cta(&ctrl->pv_done[buf], ((gs >> 1) & 1) ^ 1, p.status, abort_flag)) goto done;
           }
           if (j >= 1) {
             const int gp = g + j - 1;
-            if (!mbar_wait_cta(&ctrl->p_full, gp & 1, p.status, abort_flag)) goto done;
+            // one barrier per S buffer: the softmax may write P(gp + 1) before this wait, so a single
+            // barrier could run two phases ahead of it
+            if (!mbar_wait_cta(&ctrl->p_full[gp & 1], (gp >> 1) & 1, p.status, abort_flag)) goto done;
             // the first P V of a unit overwrites O: the previous unit's epilogue must have read it
             if (j == 1 && !mbar_wait_cta(&ctrl->o_free, (nu & 1) ^ 1, p.status, abort_flag)) goto done;
             if (!mbar_wait_cta(&ctrl->v_full[vr], vph, p.status, abort_flag)) goto done;
             tc_fence_after();
             const uint64_t vd = vdesc0 + (uint64_t)(vr * (kVSlot >> 4));
+            const uint32_t pa = tmem + kColS + (gp & 1) * kFT;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              mma_ss(to, pdesc0 + (uint64_t)((k >> 2) * (kChunk >> 4) + (k & 3) * 2), vd + (uint64_t)(k * 128),
-                     idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+              mma_ts(to, pa + k * 8, vd + (uint64_t)(k * 128), idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
             mma_commit(&ctrl->v_empty[vr]);
-            mma_commit(&ctrl->pv_done);
+            mma_commit(&ctrl->pv_done[gp & 1]);
             if (++vr == kVRing) { vr = 0; vph ^= 1; }
           }
         }
@@ -261,12 +284,20 @@ __global__ void __launch_bounds__(kFThreads, 1)
       }
     }
   } else if (warp >= 4) {
-    // softmax: thread = query row r of the unit's tile (TMEM lane r)
-    const int q4 = warp & 3, r = q4 * 32 + lane;
+    // softmax: thread = (query row r of the unit's tile = TMEM lane r, half hf of the columns)
+    const int q4 = warp & 3, r = q4 * 32 + lane, hf = (warp - 4) >> 2;
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-    uint8_t* prow = smem + kOffP + r * 128;
-    const int sw = r & 7;
-    int g = 0;
+    int g = 0, nx = 0;
+    // exchange v with the other half of the row; returns the other half's value
+    auto exchange = [&](float v, float& other) -> bool {
+      const int b = nx & 1;
+      ctrl->xval[b][hf][r] = v;
+      mbar_arrive(&ctrl->xch[b]);
+      const bool ok = warp_wait(&ctrl->xch[b], (nx >> 1) & 1, p.status, abort_flag);
+      other = ctrl->xval[b][hf ^ 1][r];
+      ++nx;
+      return ok;
+    };
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       int h, qt, n, p0;
       unit_of(p, u, h, qt, n, p0);
@@ -276,27 +307,31 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const int buf = g & 1;
         if (!warp_wait(&ctrl->s_full[buf], (g >> 1) & 1, p.status, abort_flag)) goto done;
         tc_fence_after();
-        uint32_t s[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kColS + buf * kFT + c * 32, s[c]);
+        uint32_t s[2][32];
+        tmem_ld32(lane_base + kColS + buf * kFT + hf * 64, s[0]);
+        tmem_ld32(lane_base + kColS + buf * kFT + hf * 64 + 32, s[1]);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&ctrl->s_empty[buf]);
         if (j * kFT + kFT - 1 > p0) {
           // a tile holding keys after some query of the tile: causal mask
-          const int lim = pos - j * kFT;
+          const int lim = pos - j * kFT - hf * 64;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i > lim) s[c][i] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // eight independent partial maxima, then the other half's maximum
+        float mp[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[c][i]));
-        mx *= p.scale_log2;   // the positive scale commutes with the maximum
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(s[c][i]));
+        float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        float mo;
+        if (!exchange(mx, mo)) goto done;
+        mx = fmaxf(mx, mo) * p.scale_log2;   // the positive scale commutes with the maximum
         float alpha = 1.f;
         if (j == 0) {
           m = mx;
@@ -308,59 +343,60 @@ __global__ void __launch_bounds__(kFThreads, 1)
         // the row sum adds the bf16 weights the P V MMAs use, so that the weights of the output are
         // normalised exactly: with the lazy maximum the largest weight is up to 2^8, not 1, and an fp32
         // sum of the unrounded weights would scale a row dominated by one token by its rounding error
-        uint32_t pk[64];
-        float sum0 = 0.f, sum1 = 0.f;
+        uint32_t pk[32];
+        float sp[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float e0 = ex2(fmaf(__uint_as_float(s[c][2 * i]), p.scale_log2, -m));
             const float e1 = ex2(fmaf(__uint_as_float(s[c][2 * i + 1]), p.scale_log2, -m));
             const uint32_t w = pack_bf16x2(e0, e1);
-            sum0 += __uint_as_float(w << 16);
-            sum1 += __uint_as_float(w & 0xFFFF0000u);
+            sp[(2 * i) & 7] += __uint_as_float(w << 16);
+            sp[(2 * i + 1) & 7] += __uint_as_float(w & 0xFFFF0000u);
             pk[c * 16 + i] = w;
           }
-        l += sum0 + sum1;
-        // the previous P V has read the P buffer and finished accumulating O
-        if (g >= 1 && !warp_wait(&ctrl->pv_done, (g - 1) & 1, p.status, abort_flag)) goto done;
-        tc_fence_after();
+        l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        // a larger maximum: O is rescaled once the previous P V has finished accumulating into it
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!warp_wait(&ctrl->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.status, abort_flag)) goto done;
+          tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(lane_base + kColO + c * 32, o);
+            tmem_ld32(lane_base + kColO + hf * 64 + c * 32, o);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(lane_base + kColO + c * 32, o);
+            tmem_st32(lane_base + kColO + hf * 64 + c * 32, o);
           }
           tmem_st_wait();
         }
-        // P row r: keys 64 ch .. 64 ch + 63 in chunk ch, 16-byte unit uu (keys 8 uu .. 8 uu + 7) at the
-        // 128-byte swizzled position uu ^ (r & 7)
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-          for (int uu = 0; uu < 8; ++uu)
-            *reinterpret_cast<uint4*>(prow + ch * kChunk + ((uu ^ sw) << 4)) =
-                make_uint4(pk[ch * 32 + 4 * uu], pk[ch * 32 + 4 * uu + 1], pk[ch * 32 + 4 * uu + 2],
-                           pk[ch * 32 + 4 * uu + 3]);
-        fence_proxy_async_smem();
+        // P row r, keys 64 hf .. 64 hf + 63, as bf16 pairs into columns 32 hf .. 32 hf + 31 of this tile's
+        // S buffer (the exchange above ordered it after both halves' loads of S)
+        tmem_st32(lane_base + kColS + buf * kFT + hf * 32, pk);
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&ctrl->p_full);
+        mbar_arrive(&ctrl->p_full[buf]);
       }
-      // epilogue: O / l in bf16, and the log-sum-exp of the row
-      if (!warp_wait(&ctrl->pv_done, (g - 1) & 1, p.status, abort_flag)) goto done;
+      // epilogue: the full row sum, then O / l in bf16 (this half's 64 columns) and the log-sum-exp
+      {
+        float lo;
+        if (!exchange(l, lo)) goto done;
+        l += lo;
+      }
+      if (!warp_wait(&ctrl->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, p.status, abort_flag)) goto done;
       tc_fence_after();
       {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int q = qt * kFT + r;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + ((long long)q * p.H + h) * kVH);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + ((long long)q * p.H + h) * kVH + hf * 64);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_base + kColO + c * 32, o);
+          tmem_ld32(lane_base + kColO + hf * 64 + c * 32, o);
           tmem_ld_wait();
           if (q < p.T) {
 #pragma unroll
@@ -373,7 +409,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
           }
         }
-        if (q < p.T && p.lse) p.lse[(long long)q * p.H + h] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        if (hf == 0 && q < p.T && p.lse) p.lse[(long long)q * p.H + h] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
       }
       tc_fence_before();
       mbar_arrive(&ctrl->o_free);
@@ -435,12 +471,11 @@ cudaError_t tc_prefill_attention(const Ctx& ctx, const mla_config* cfg, const vo
   if (e != cudaSuccess) return e;
   CUtensorMap mapq, mapkv, mapr;
   const uint64_t dq[3] = {(uint64_t)kQW, (uint64_t)H, (uint64_t)T}, sq[2] = {(uint64_t)kQW * 2, (uint64_t)H * kQW * 2};
-  const uint64_t dkv[3] = {(uint64_t)kQK, (uint64_t)2 * H, (uint64_t)L},
-                 skv[2] = {(uint64_t)kQK * 2, (uint64_t)2 * H * kQK * 2};
-  const uint64_t dr[2] = {(uint64_t)kRowW, (uint64_t)L}, sr[1] = {(uint64_t)kRowW * 2};
-  const uint32_t box3[3] = {64, 1, kFT}, box2[2] = {64, kFT};
-  if (!encode_map_bf16(&mapq, q, 3, dq, sq, box3) || !encode_map_bf16(&mapkv, kv, 3, dkv, skv, box3) ||
-      !encode_map_bf16(&mapr, lat, 2, dr, sr, box2))
+  const uint64_t dkv[3] = {64, (uint64_t)L, (uint64_t)4 * H}, skv[2] = {128, (uint64_t)L * 128};
+  const uint64_t dr[3] = {64, (uint64_t)L, (uint64_t)kRowW / 64}, sr[2] = {128, (uint64_t)L * 128};
+  const uint32_t boxq[3] = {64, 1, kFT}, boxc[3] = {64, kFT, 1};
+  if (!encode_map_bf16(&mapq, q, 3, dq, sq, boxq) || !encode_map_bf16(&mapkv, kv, 3, dkv, skv, boxc) ||
+      !encode_map_bf16(&mapr, lat, 3, dr, sr, boxc))
     return cudaErrorInvalidValue;
   FParams fp;
   fp.T = T;
