@@ -47,14 +47,16 @@ def decode_algorithmic(p: I.Problem) -> dict:
     * elem bytes, read once for all heads and both queries), and
     2 * H * (d_c + d_rope + d_c) FLOPs (scores over the full row, weighted sum
     over the latent).  Per query row: q read and o_lat written.  Block table:
-    4 B per 64-token block."""
+    4 B per 64-token block.  A reduced-precision cache row is d_c + 2 d_rope + 4
+    bytes (codes, bf16 key divided by the scale, fp32 scale)."""
     d = p.dims
     eb = 2 if p.w.dtype == "bf16" else 4
     kv = p.kv_len.astype(np.int64)
     n_q = p.w.n_q
     rows = int(kv.sum())
     vis = int(sum(max(0, int(k) - (n_q - 1 - j)) for k in kv for j in range(n_q)))
-    latent_bytes = rows * d.row * eb
+    row_bytes = d.d_c + 2 * d.d_rope + 4 if getattr(p.w, "cache_fp8", False) else d.row * eb
+    latent_bytes = rows * row_bytes
     q_bytes = p.w.batch * n_q * d.n_heads * d.row * eb
     o_bytes = p.w.batch * n_q * d.n_heads * d.d_c * eb
     table_bytes = int(sum((int(k) + d.block_size - 1) // d.block_size for k in kv)) * 4

@@ -87,6 +87,7 @@ typedef struct {
   int block_size;      /* tokens per cache block; 64 */
   float softmax_scale;
   int dtype;           /* mla_dtype */
+  int cache_fp8;       /* 0: cache rows in dtype; 1: reduced-precision cache (bf16 only, see below) */
 } mla_config;
 
 /* Paged latent cache.  Each token's row is [c_KV || k_R], d_c + d_rope values
@@ -98,7 +99,19 @@ typedef struct {
  *   pool: [num_blocks][d_c + d_rope][block_size] of dtype, element e of that
  *   token at pool[(k * (d_c + d_rope) + e) * block_size + o].
  * (Element-major blocks let the decode kernel fetch whole contiguous runs of a
- * block per copy and feed them to the tensor cores as either operand layout.) */
+ * block per copy and feed them to the tensor cores as either operand layout.)
+ *
+ * Reduced-precision cache (cache_fp8 = 1, dtype bf16; [KJ "Compression as
+ * architecture versus compression as post-processing"]: a latent can itself be
+ * stored in a reduced-precision format).  The format is this library's (the
+ * pages name none): the latent of a token is stored as FP8 E4M3 codes of
+ * c_t / s_t, s_t the smallest power of two with max|c_t| / s_t <= 448 (1 for
+ * an all-zero row), rounded to nearest even; the positional key as bf16 values
+ * of k_R,t / s_t (exact: s_t is a power of two); s_t as fp32.  A block holds
+ * block_size * (d_c + 2 d_rope + 4) bytes, element-major per part:
+ *   codes  [d_c][block_size] bytes at block offset 0,
+ *   k_R/s  [d_rope][block_size] bf16 at block offset d_c * block_size,
+ *   s      [block_size] fp32 at block offset (d_c + 2 d_rope) * block_size. */
 typedef struct {
   void* pool;                   /* device */
   int num_blocks;
@@ -113,7 +126,8 @@ typedef struct {
   int max_pos;
 } mla_rope_table;
 
-/* Bytes one token occupies in the cache: (d_c + d_rope) * sizeof(dtype).
+/* Bytes one token occupies in the cache: (d_c + d_rope) * sizeof(dtype), or
+ * d_c + 2 d_rope + 4 for the reduced-precision cache (644 at the DeepSeek-V2 shape).
  * [TM "Key Problems Solved"]: the per-token cache shrinks from 2*H*d to the
  * latent; [SC]: plus the positional part.  Returns 0 for an invalid config. */
 size_t mla_cache_bytes_per_token(const mla_config* cfg);
@@ -140,6 +154,8 @@ size_t mla_compress_workspace_bytes(const mla_config* cfg, int T);
  *   seq_idx, pos  device int32 [T]
  *   rope   table covering every pos[t]
  *   cache  the paged cache; only the T addressed rows are written
+ * With cache_fp8 the row is quantised as described above (one scale per token,
+ * from the row's fp32 values).
  * A token whose seq_idx, pos or block id is out of range is skipped and
  * flagged (MLA_ERR_DEVICE_INDEX via mla_get_device_status). */
 mla_status mla_compress_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
@@ -181,6 +197,10 @@ size_t mla_decode_workspace_bytes(const mla_config* cfg, int batch, int n_q, int
  *           softmax normaliser of the scaled scores; -inf when nothing is
  *           visible), or NULL
  * A query with no visible token gets o_lat = 0.
+ * With cache_fp8 the call first expands the visited blocks of every sequence
+ * into bf16 rows (codes * s, (k_R / s) * s: exact) in the workspace and then
+ * attends over them; the workspace grows by batch * max_blocks_per_seq bf16
+ * blocks.
  * Reproducibility: on the tensor-core path each 128-token score tile sums its
  * six 96-element slices in a fixed order, so repeated calls on the same inputs
  * and GPU give the same bits; another SM count or batch moves the split points
@@ -247,7 +267,7 @@ size_t mla_prefill_workspace_bytes(const mla_config* cfg, int kv_len);
  *   lse    optional device fp32 [T][n_heads] (natural log of the softmax
  *          normaliser of the scaled scores), or NULL
  * 1 <= T <= kv_len.  Block-table entries outside the pool read as zero rows
- * and are flagged.  Three launches: the latent gather, the K/V GEMM, the
+ * and are flagged.  With cache_fp8 the gather expands the rows to bf16.  Three launches: the latent gather, the K/V GEMM, the
  * attention kernel. */
 mla_status mla_prefill_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache, int seq,
                                  int kv_len, int T, const void* W_UK, const void* W_UV, void* o, float* lse,

@@ -29,10 +29,17 @@ class DeviceLayer:
         w, d = p.w, p.dims
         self.device = device
         self.dt = tdtype(w.dtype)
-        self.cfg = M.make_config(d, w.dtype)
+        self.fp8 = bool(getattr(w, "cache_fp8", False))
+        self.cfg = M.make_config(d, w.dtype, cache_fp8=self.fp8)
         self.W = {k: to_dev(v, w.dtype, device) for k, v in p.weights.items()}
-        # each block stored transposed: [row element][block_size tokens]; NaN sentinels everywhere unwritten
-        self.pool = torch.full((p.num_blocks, d.row, d.block_size), float("nan"), dtype=self.dt, device=device)
+        if self.fp8:
+            # reduced-precision blocks as raw bytes: codes [d_c][bs], k_R / s [d_rope][bs] bf16, s [bs] fp32;
+            # 0xFF everywhere unwritten (a NaN code, a NaN bf16, a NaN scale)
+            self.fp8_block_bytes = d.block_size * (d.d_c + 2 * d.d_rope + 4)
+            self.pool = torch.full((p.num_blocks, self.fp8_block_bytes), 255, dtype=torch.uint8, device=device)
+        else:
+            # each block stored transposed: [row element][block_size tokens]; NaN sentinels everywhere unwritten
+            self.pool = torch.full((p.num_blocks, d.row, d.block_size), float("nan"), dtype=self.dt, device=device)
         self.block_table = torch.from_numpy(p.block_table).to(device)
         if max_pos is None:
             max_pos = int(p.block_table.shape[1]) * d.block_size + 8
@@ -55,10 +62,34 @@ class DeviceLayer:
         self.ws = {}
 
     # ---------------------------------------------------------------- cache fill
+    def fp8_parts(self):
+        """Views of the reduced-precision pool: codes [nb, d_c, bs] uint8, k_R / s [nb, d_rope, bs] bf16,
+        s [nb, bs] fp32."""
+        d = self.p.dims
+        bs, nb = d.block_size, self.pool.shape[0]
+        codes = self.pool[:, :d.d_c * bs].view(nb, d.d_c, bs)
+        kr = self.pool[:, d.d_c * bs:(d.d_c + 2 * d.d_rope) * bs].view(torch.bfloat16).view(nb, d.d_rope, bs)
+        sc = self.pool[:, (d.d_c + 2 * d.d_rope) * bs:].view(torch.float32).view(nb, bs)
+        return codes, kr, sc
+
     def fill_direct(self):
         """Write drawn latent rows at every cached position (no projection involved)."""
         p, d = self.p, self.p.dims
         bs = d.block_size
+        if self.fp8:
+            codes_v, kr_v, sc_v = self.fp8_parts()
+            for b in range(p.w.batch):
+                L = int(p.lens[b])
+                if L == 0:
+                    continue
+                codes, k, kr = I.draw_fp8_rows(p.w, b, L)
+                pos = np.arange(L)
+                blk = torch.from_numpy(p.block_table[b, pos // bs].astype(np.int64)).to(self.device)
+                off = torch.from_numpy(pos % bs).to(self.device)
+                codes_v[blk, :, off] = torch.from_numpy(codes).to(self.device)
+                kr_v[blk, :, off] = torch.from_numpy(kr).to(self.device, torch.bfloat16)
+                sc_v[blk, off] = torch.from_numpy(np.ldexp(np.float32(1.0), k).astype(np.float32)).to(self.device)
+            return
         for b in range(p.w.batch):
             L = int(p.lens[b])
             if L == 0:
@@ -143,11 +174,16 @@ class DeviceLayer:
         return raw.transpose(1, 2).cpu().numpy()
 
     def cache_rows_at(self, seq, pos) -> np.ndarray:
-        """Rows at logical positions pos[i] of sequences seq[i], read back from the pool (float32 numpy)."""
+        """Rows at logical positions pos[i] of sequences seq[i], read back from the pool (float32 numpy).
+        For a reduced-precision pool: (codes uint8 [n, d_c], k_R / s float32 [n, d_rope], s float32 [n])."""
         bs = self.p.dims.block_size
         seq, pos = np.asarray(seq, dtype=np.int64), np.asarray(pos, dtype=np.int64)
         blk = torch.from_numpy(self.p.block_table[seq, pos // bs].astype(np.int64)).to(self.device)
         off = torch.from_numpy(pos % bs).to(self.device)
+        if self.fp8:
+            codes, kr, sc = self.fp8_parts()
+            return (codes[blk, :, off].cpu().numpy(), kr[blk, :, off].float().cpu().numpy(),
+                    sc[blk, off].cpu().numpy())
         return self.pool[blk, :, off].float().cpu().numpy()
 
     def cache_rows_logical(self, b: int, n: int | None = None) -> np.ndarray:
@@ -176,9 +212,13 @@ class PrefillLayer:
         c, d = p.case, p.dims
         self.device = device
         self.dt = tdtype(c.dtype)
-        self.cfg = M.make_config(d, c.dtype)
+        self.cfg = M.make_config(d, c.dtype, cache_fp8=c.cache_fp8)
         self.W = {k: to_dev(v, c.dtype, device) for k, v in p.weights.items()}
-        self.pool = torch.full((p.num_blocks, d.row, d.block_size), float("nan"), dtype=self.dt, device=device)
+        if c.cache_fp8:
+            self.pool = torch.full((p.num_blocks, d.block_size * (d.d_c + 2 * d.d_rope + 4)), 255, dtype=torch.uint8,
+                                   device=device)
+        else:
+            self.pool = torch.full((p.num_blocks, d.row, d.block_size), float("nan"), dtype=self.dt, device=device)
         self.block_table = torch.from_numpy(p.block_table).to(device)
         self.cache = M.make_cache(self.pool, self.block_table, d.block_size)
         max_pos = int(p.block_table.shape[1]) * d.block_size + 8

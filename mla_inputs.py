@@ -70,6 +70,7 @@ class Workload:
     seed: int
     fill: str             # "append": cache built with compress_append; "direct": latent rows drawn
     note: str = ""
+    cache_fp8: bool = False   # reduced-precision cache (FP8 E4M3 latent codes, per-token scale)
 
     @property
     def fixed_len(self) -> bool:
@@ -91,6 +92,11 @@ WORKLOADS = {
                  "long context, split-KV"),
         Workload("dsv2_b128_ctx4k_32k_nq2", DSV2, "bf16", 128, 4096, 32768, 2, 2, 5, "direct",
                  "two new tokens appended, causal between them"),
+        Workload("dsv2_b64_ctx8192_fp8", DSV2, "bf16", 64, 8191, 8191, 1, 1, 34, "direct",
+                 "the decode step over a reduced-precision cache (drawn codes, scales and keys; the new "
+                 "token quantised by the append)", cache_fp8=True),
+        Workload("dsv2_b16_ctx4096_fp8", DSV2, "bf16", 16, 4096, 4096, 1, 0, 35, "append",
+                 "reduced-precision cache built by appending 65,536 tokens", cache_fp8=True),
     ]
 }
 
@@ -160,6 +166,23 @@ def draw_latent_rows(w: Workload, b: int, n_rows: int) -> np.ndarray:
     """Directly drawn cache rows [n_rows, d_c + d_rope] for sequence b (its own sub-stream)."""
     rng = np.random.default_rng([w.seed, 1000 + b])
     return storage(_normal(rng, (n_rows, w.dims.row), 1.0), w.dtype)
+
+
+def draw_fp8_rows(w: Workload, b: int, n_rows: int):
+    """Directly drawn rows of a reduced-precision cache for sequence b (its own sub-stream): latent
+    codes as FP8 E4M3 bit patterns (random sign, exponent field 6..14, mantissa 0..7: magnitudes
+    0.5..480 before the scale), the per-token scale exponent k (uniform in -9..-7; scale 2^k) and the
+    stored positional key k_R / 2^k (bf16 values of a Gaussian of standard deviation 2^-k, so that the
+    key itself has unit spread).  Returns (codes uint8 [n, d_c], k int [n], kr_scaled float32 [n, d_rope])."""
+    d = w.dims
+    rng = np.random.default_rng([w.seed, 2000 + b])
+    sign = rng.integers(0, 2, size=(n_rows, d.d_c)) << 7
+    expo = rng.integers(6, 15, size=(n_rows, d.d_c)) << 3
+    mant = rng.integers(0, 8, size=(n_rows, d.d_c))
+    codes = (sign | expo | mant).astype(np.uint8)
+    k = rng.integers(-9, -6, size=n_rows)
+    kr = _normal(rng, (n_rows, d.d_rope), 1.0) * (2.0 ** -k)[:, None].astype(np.float32)
+    return codes, k.astype(np.int32), round_to_bf16(kr)
 
 
 def draw_block_table(capacity: np.ndarray, block_size: int, rng: np.random.Generator,
@@ -244,6 +267,7 @@ class PrefillCase:
     others: tuple = (100, 37)
     seq: int = 1
     note: str = ""
+    cache_fp8: bool = False   # reduced-precision cache (fill "append" only)
 
 
 PREFILL_CASES = {
@@ -260,6 +284,8 @@ PREFILL_CASES = {
         PrefillCase("prefill_dsv2_L4096_T4096", DSV2, "bf16", 4096, 4096, 46,
                     note="a 4096-token prompt (benchmark size)"),
         PrefillCase("prefill_dsv2_L8192_T8192", DSV2, "bf16", 8192, 8192, 47, note="an 8192-token prompt"),
+        PrefillCase("prefill_dsv2_L333_T200_x_fp8", DSV2, "bf16", 333, 200, 48, fill="append", cache_fp8=True,
+                    note="from hidden states over a reduced-precision cache"),
     ]
 }
 

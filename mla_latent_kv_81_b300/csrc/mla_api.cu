@@ -86,6 +86,8 @@ mla_status check_cfg(const mla_config* c) {
       c->block_size <= 0)
     return MLA_ERR_INVALID_ARG;
   if (c->dtype != MLA_F32 && c->dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+  if (c->cache_fp8 != 0 && c->cache_fp8 != 1) return MLA_ERR_INVALID_ARG;
+  if (c->cache_fp8 && c->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
   if (c->d_rope % 2) return MLA_ERR_UNSUPPORTED;
   if (c->d_c > 512 || c->d_c + c->d_rope > 2048) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
@@ -243,6 +245,7 @@ const char* mla_status_string(mla_status s) {
 
 size_t mla_cache_bytes_per_token(const mla_config* cfg) {
   if (check_cfg(cfg) != MLA_OK) return 0;
+  if (cfg->cache_fp8) return (size_t)cfg->d_c + 2 * (size_t)cfg->d_rope + 4;
   return (size_t)(cfg->d_c + cfg->d_rope) * elem_size(cfg->dtype);
 }
 
@@ -335,7 +338,8 @@ size_t mla_decode_workspace_bytes(const mla_config* cfg, int batch, int n_q, int
   const int sms = current_sm_count();
   if (cfg->dtype == MLA_BF16) {
     if (!tc_decode_supported(cfg, batch, n_q)) return 0;
-    return kWsHeader + tc_decode_workspace_bytes(cfg, batch, n_q, max_blocks_per_seq, sms);
+    return kWsHeader + align_up(tc_decode_workspace_bytes(cfg, batch, n_q, max_blocks_per_seq, sms), 256) +
+           (cfg->cache_fp8 ? fp8_expand_bytes(cfg, batch, max_blocks_per_seq) : 0);
   }
   return kWsHeader + simt_decode_ws(cfg, batch, n_q, max_blocks_per_seq, sms);
 }
@@ -356,6 +360,15 @@ mla_status mla_decode_attention(const mla_config* cfg, const void* q, const mla_
   MLA_TRY(device_ctx(stream, workspace, &ctx));
   const float scale = resolve_scale(cfg);
   if (cfg->dtype == MLA_BF16) {
+    if (cfg->cache_fp8) {
+      // the visited blocks expanded to bf16 rows in the workspace, then the same attention kernel
+      char* scratch = ws_body(workspace) +
+                      align_up(tc_decode_workspace_bytes(cfg, batch, n_q, cache->max_blocks_per_seq, ctx.sm_count), 256);
+      mla_paged_cache expanded;
+      MLA_CUDA(launch_expand_fp8(ctx, cfg, *cache, kv_len, batch, scratch, &expanded));
+      MLA_CUDA(tc_decode_attention(ctx, cfg, q, expanded, kv_len, batch, n_q, scale, o_lat, lse, ws_body(workspace)));
+      return MLA_OK;
+    }
     MLA_CUDA(tc_decode_attention(ctx, cfg, q, *cache, kv_len, batch, n_q, scale, o_lat, lse, ws_body(workspace)));
     return MLA_OK;
   }

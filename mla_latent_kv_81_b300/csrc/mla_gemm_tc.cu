@@ -565,6 +565,9 @@ cudaError_t tc_compress_append(const Ctx& ctx, const mla_config* cfg, const void
     return cudaErrorInvalidValue;
   cudaError_t e = launch_gemm(ctx, a1, a2, b, pl);
   if (e != cudaSuccess) return e;
+  if (cfg->cache_fp8)
+    return launch_compress_reduce_fp8(ctx, pl.args.partial, pl.args.splits, T, d_c, d_r, seq_idx, pos, rope, cache,
+                                      cfg->block_size);
   const int width = d_c + d_r;
   dim3 grid((T + kAppTok - 1) / kAppTok, (width + kAppCols - 1) / kAppCols);
   compress_reduce_kernel<<<grid, 256, 0, ctx.stream>>>(pl.args.partial, pl.args.splits, T, d_c, d_r, seq_idx, pos,

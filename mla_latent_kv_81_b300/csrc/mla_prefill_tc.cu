@@ -460,12 +460,17 @@ cudaError_t tc_prefill_attention(const Ctx& ctx, const mla_config* cfg, const vo
   char* base = static_cast<char*>(workspace);
   bf16* lat = reinterpret_cast<bf16*>(base + w.lat);
   bf16* kv = reinterpret_cast<bf16*>(base + w.kv);
-  const dim3 gg((L + kFBlk - 1) / kFBlk, kRowW / 64);
-  gather_latent_kernel<<<gg, 256, 0, ctx.stream>>>(static_cast<const bf16*>(cache.pool), cache.block_table,
-                                                   cache.max_blocks_per_seq, cache.num_blocks, seq, L, lat,
-                                                   ctx.status);
-  count_launch();
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (cfg->cache_fp8) {
+    e = launch_gather_latent_fp8(ctx, cfg, cache, seq, L, lat);
+  } else {
+    const dim3 gg((L + kFBlk - 1) / kFBlk, kRowW / 64);
+    gather_latent_kernel<<<gg, 256, 0, ctx.stream>>>(static_cast<const bf16*>(cache.pool), cache.block_table,
+                                                     cache.max_blocks_per_seq, cache.num_blocks, seq, L, lat,
+                                                     ctx.status);
+    count_launch();
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   e = tc_reconstruct_kv(ctx, cfg, lat, L, W_UK, W_UV, kv);
   if (e != cudaSuccess) return e;

@@ -48,6 +48,21 @@ size_t tc_head_output_workspace_bytes(const mla_config* cfg, int N, int sm_count
 cudaError_t tc_head_output_project(const Ctx& ctx, const mla_config* cfg, const void* o, const void* W_O, void* out,
                                    int N, void* workspace);
 
+// Reduced-precision latent cache (FP8 E4M3 codes with a power-of-two scale per token).
+// The append's epilogue from the k-split partials of the stacked W_DKV / W_KR GEMM.
+cudaError_t launch_compress_reduce_fp8(const Ctx& ctx, const float* part, int splits, int T, int d_c, int d_r,
+                                       const int32_t* seq_idx, const int32_t* pos, const mla_rope_table& rope,
+                                       const mla_paged_cache& cache, int block_size);
+// Scratch for the decode: batch * max_blocks bf16 blocks and their block table.
+size_t fp8_expand_bytes(const mla_config* cfg, int batch, int max_blocks);
+// Expand the visited blocks of every sequence into bf16 blocks in `scratch`; *expanded describes them
+// as a bf16 paged cache (block b * max_blocks + k holds logical block k of sequence b).
+cudaError_t launch_expand_fp8(const Ctx& ctx, const mla_config* cfg, const mla_paged_cache& cache,
+                              const int32_t* kv_len, int batch, void* scratch, mla_paged_cache* expanded);
+// Prefill: sequence seq's first L rows expanded to bf16 into the chunk-major lat[(d_c + d_rope) / 64][L][64].
+cudaError_t launch_gather_latent_fp8(const Ctx& ctx, const mla_config* cfg, const mla_paged_cache& cache, int seq,
+                                     int L, void* lat);
+
 // bf16 tensor map of rank 1..5 with the 128-byte swizzle: dims[0] innermost, strides[i] the byte
 // stride of dimension i + 1, box the copied extent per dimension.
 bool encode_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,

@@ -323,6 +323,58 @@ def decode_layer_absorbed(x_q, q_pos, caches, W, dims, n_q: int, kv_len):
     return output_project(up_project_values(o_lat, W["W_UV"]), W["W_O"])
 
 
+# ------------------------------------------------------------------ reduced-precision latent cache
+# [KJ "Compression as architecture versus compression as post-processing"]: a latent representation
+# can itself be stored in a reduced-precision format.  Reading c21 (the pages name no format): FP8 E4M3
+# codes (4 exponent bits, bias 7, 3 mantissa bits, subnormals below 2^-6, largest finite 448) of
+# c_t / s_t with one power-of-two scale s_t per token, the smallest with max|c_t| / s_t <= 448; the
+# positional key is kept in bf16, stored divided by the same s_t (exact for a power of two).
+E4M3_MAX = 448.0
+
+
+def round_e4m3(x) -> np.ndarray:
+    """Nearest FP8 E4M3 value of each element (ties to even), for |x| <= 448.
+
+    Normal values 2^e (1 + m/8), e >= -6, have spacing 2^(e-3); below 2^-6 the spacing is 2^-9."""
+    x = _a(x)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    q = 2.0 ** (np.maximum(e, -6.0) - 3.0)
+    return np.sign(x) * np.round(a / q) * q          # numpy rounds halves to even
+
+
+def e4m3_value(code) -> np.ndarray:
+    """The value of each FP8 E4M3 bit pattern (uint8): sign, 4-bit exponent (bias 7), 3-bit mantissa;
+    exponent 0 is subnormal (m/8 * 2^-6); pattern 0x7F / 0xFF (NaN) gives nan."""
+    c = np.asarray(code, dtype=np.int64)
+    sgn = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    return np.where((c & 0x7F) == 0x7F, np.nan, sgn * val)
+
+
+def fp8_token_scale(c) -> np.ndarray:
+    """Reading c21: per token (last axis) the smallest power of two s with max|c| / s <= 448; 1 when
+    the row is all zeros."""
+    m = np.max(np.abs(_a(c)), axis=-1)
+    k = np.ceil(np.log2(np.where(m > 0, m, E4M3_MAX) / E4M3_MAX))
+    return 2.0 ** k
+
+
+def quantize_latent_fp8(c, k_r):
+    """A cache row in the reduced-precision format (reading c21): returns (codes as values, s, k_R / s
+    rounded to bf16).  The stored latent is codes * s, the stored positional key (k_R / s) * s."""
+    c, k_r = _a(c), _a(k_r)
+    s = fp8_token_scale(c)
+    return round_e4m3(c / s[..., None]), s, round_bf16(k_r / s[..., None])
+
+
+def dequantize_latent_fp8(codes, s, k_r_scaled):
+    """Latent and positional key a reduced-precision cache row stands for: (codes * s, k_R' * s)."""
+    s = _a(s)[..., None]
+    return _a(codes) * s, _a(k_r_scaled) * s
+
+
 # ------------------------------------------------------------------ cache-size closed forms
 def kv_cache_elems_per_token(n_kv_heads: int, d_head: int, n_layers: int = 1) -> int:
     """Head-sharing / MHA cache: keys and values per KV head, 2 * H_kv * d per layer.

@@ -63,15 +63,23 @@ def logical_cache(p: I.Problem, b: int):
     then the appended query tokens projected from x_q."""
     d = p.dims
     L = int(p.lens[b])
-    if p.w.fill == "direct":
+    fp8 = getattr(p.w, "cache_fp8", False)
+    if p.w.fill == "direct" and fp8:
+        codes, k, kr = I.draw_fp8_rows(p.w, b, L)
+        c, k_r = O.dequantize_latent_fp8(O.e4m3_value(codes), 2.0 ** k, kr)
+    elif p.w.fill == "direct":
         rows = I.draw_latent_rows(p.w, b, L).astype(np.float64)
         c, k_r = rows[:, :d.d_c], rows[:, d.d_c:]
     else:
         start = int(p.lens[:b].sum())
         c, k_r = O.compress(p.x_ctx[start:start + L], p.weights["W_DKV"], p.weights["W_KR"], np.arange(L), d.rope_base)
+        if fp8:
+            c, k_r = O.dequantize_latent_fp8(*O.quantize_latent_fp8(c, k_r))
     if p.w.n_append:
         sl = slice(b * p.w.n_q, (b + 1) * p.w.n_q)
         c2, r2 = O.compress(p.x_q[sl], p.weights["W_DKV"], p.weights["W_KR"], p.q_pos[sl], d.rope_base)
+        if fp8:
+            c2, r2 = O.dequantize_latent_fp8(*O.quantize_latent_fp8(c2, r2))
         c, k_r = np.concatenate([c, c2]), np.concatenate([k_r, r2])
     return c, k_r
 

@@ -198,6 +198,41 @@ def check_prefill_rows(seed, d_model, H, qk_nope, d_rope, v_head, d_c, L, pos, t
         assert np.max(np.abs(lse[j] - lse_abs[0])) <= 1e-10
 
 
+def check_fp8_format(seed=12):
+    """The reduced-precision cache format (reading c21) against torch's float8_e4m3fn: rounding of
+    50,000 values over the whole range (with exact ties and subnormals), the value of every bit
+    pattern, and the scale rule (max |c| / s in (224, 448], s a power of two)."""
+    import torch
+    rng = np.random.default_rng(seed)
+    x = np.concatenate([
+        rng.uniform(-448, 448, 20000),
+        np.sign(rng.standard_normal(20000)) * 2.0 ** rng.uniform(-12, 8.8, 20000),
+        # exact ties: midpoints between neighbouring codes (normal and subnormal)
+        (np.arange(1, 64) + 0.5) * 2.0 ** -9, (8 + np.arange(0, 8) + 0.5) * 2.0 ** -3 * 2.0 ** 4,
+        [0.0, 448.0, -448.0, 2.0 ** -6, 2.0 ** -9, 1.5 * 2.0 ** -10],
+    ])
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    exact32 = x.astype(np.float32).astype(np.float64) == x     # torch converts from float32
+    got = O.round_e4m3(x)
+    assert np.array_equal(got[exact32], ref[exact32])
+    codes = np.arange(256, dtype=np.uint8)
+    tv = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ov = O.e4m3_value(codes)
+    assert np.array_equal(np.isnan(ov), np.isnan(tv)) and np.array_equal(ov[~np.isnan(ov)], tv[~np.isnan(tv)])
+    rows = rng.standard_normal((500, 64)) * 2.0 ** rng.uniform(-30, 30, (500, 1))
+    sc = O.fp8_token_scale(rows)
+    ratio = np.max(np.abs(rows), axis=1) / sc
+    assert np.all(ratio <= 448) and np.all(ratio > 224)
+    assert np.all(np.log2(sc) == np.round(np.log2(sc)))
+    assert O.fp8_token_scale(np.zeros((1, 8)))[0] == 1.0
+    # round trip: every code of the row's range stands for itself; the error is at most half a spacing
+    codes_v, s, _ = O.quantize_latent_fp8(rows, rows[:, :4])
+    assert np.all(np.abs(codes_v) <= 448)
+    err = np.abs(codes_v * s[:, None] - rows)
+    assert np.all(err <= 2.0 ** -4 * np.abs(rows) + 2.0 ** -10 * s[:, None])
+
+
 def check_rope_properties(d_rope=16, base=10000.0):
     rng = np.random.default_rng(7)
     v = rng.standard_normal((5, d_rope))

@@ -41,6 +41,15 @@ def test_cache_bytes_per_token_matches_closed_form():
         assert M.mla_cache_bytes_per_token(cfg) == expect
     assert M.mla_cache_bytes_per_token(M.make_config(I.DSV2, "bf16")) == 1152
     assert M.mla_cache_bytes_per_token(M.make_config(I.TINY, "f32")) == 320
+    # reduced-precision cache (reading c21): one byte per latent element, bf16 key, fp32 scale
+    assert M.mla_cache_bytes_per_token(M.make_config(I.DSV2, "bf16", cache_fp8=True)) == 512 + 2 * 64 + 4
+    assert M.mla_cache_bytes_per_token(M.make_config(I.TINY, "f32", cache_fp8=True)) == 0   # bf16 only
+    bad = M.make_config(I.DSV2, "bf16")
+    bad.cache_fp8 = 2
+    assert M.mla_cache_bytes_per_token(bad) == 0
+    # the decode workspace of a reduced-precision cache also holds the expanded bf16 blocks
+    f8 = M.make_config(I.DSV2, "bf16", cache_fp8=True)
+    assert M.mla_decode_workspace_bytes(f8, 4, 1, 10) >= M.mla_decode_workspace_bytes(cfg := M.make_config(I.DSV2, "bf16"), 4, 1, 10) + 40 * 576 * 64 * 2
 
 
 def test_invalid_config_is_rejected():

@@ -48,6 +48,10 @@ def test_prefill_rows_against_sdpa(shape):
     pins.check_prefill_rows(seed=6, **shape)
 
 
+def test_fp8_cache_format():
+    pins.check_fp8_format()
+
+
 def test_rope_properties():
     pins.check_rope_properties(16)
     pins.check_rope_properties(64)

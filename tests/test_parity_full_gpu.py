@@ -21,7 +21,24 @@ from oracle import mla_oracle as O
 pytestmark = pytest.mark.gpu
 
 FULL = ["dsv2_b16_ctx4096", "dsv2_b64_ctx1k_8k", "dsv2_b64_ctx8192", "dsv2_b4_ctx65536",
-        "dsv2_b128_ctx4k_32k_nq2"]
+        "dsv2_b128_ctx4k_32k_nq2", "dsv2_b64_ctx8192_fp8"]
+
+
+def assert_fp8_rows_close(got, x, W_DKV, W_KR, pos, base, what):
+    """Reduced-precision rows read back (codes, k_R / s, s) against the oracle's quantiser of its own
+    float64 rows: the dequantised latent within one code spacing times the scale (a code or scale may
+    differ from the oracle's where the float64 value lies within fp32 rounding of a decision
+    boundary; test_fp8_gpu checks the exact cases), the positional key within one bf16 ulp."""
+    codes, kr_s, s = got
+    c, k_r = O.compress(np.asarray(x, dtype=np.float64), W_DKV, W_KR, pos, base)
+    cq, kq = O.dequantize_latent_fp8(*O.quantize_latent_fp8(c, k_r))
+    cg = O.e4m3_value(codes) * s[:, None]
+    assert np.all(np.isfinite(cg)), what
+    smax = np.maximum(s, O.fp8_token_scale(c))[:, None]
+    spacing = 2.0 ** (np.maximum(np.floor(np.log2(np.maximum(np.abs(cq) / smax, 1e-30))), -6.0) - 3.0) * smax
+    assert np.all(np.abs(cg - cq) <= spacing + 1e-30), what
+    kg = kr_s * s[:, None]
+    assert np.all(np.abs(kg - kq) <= 2.0 ** (np.floor(np.log2(np.maximum(np.abs(kq), 1e-30))) - 7) + 1e-30), what
 
 
 def samples(p: I.Problem):
@@ -66,10 +83,11 @@ def test_full_size_step(name):
         ref = oracle_sequence(p, b, explicit=(i == 0 and int(p.kv_len[b]) <= 16384))
         assert_close(out[b * n_q:(b + 1) * n_q], ref["out"], "bf16", f"{name} out b={b}")
 
-    # appended cache rows (reading c13)
+    # appended cache rows (reading c13; reduced-precision rows within one code spacing, reading c21)
+    check_rows = assert_fp8_rows_close if p.w.cache_fp8 else assert_append_c13
     if p.w.n_append:
         rows = L.cache_rows_at(np.repeat(np.arange(p.w.batch), n_q), p.q_pos)
-        assert_append_c13(rows, p.x_q, W["W_DKV"], W["W_KR"], p.q_pos, d.rope_base, f"{name} appended rows")
+        check_rows(rows, p.x_q, W["W_DKV"], W["W_KR"], p.q_pos, d.rope_base, f"{name} appended rows")
     if p.w.fill == "append":
         rng = np.random.default_rng(p.w.seed + 100)
         starts = np.concatenate([[0], np.cumsum(p.lens)[:-1]])
@@ -77,4 +95,4 @@ def test_full_size_step(name):
         seq = np.searchsorted(starts, pick, side="right") - 1
         pos = pick - starts[seq]
         got = L.cache_rows_at(seq, pos)
-        assert_append_c13(got, p.x_ctx[pick], W["W_DKV"], W["W_KR"], pos, d.rope_base, f"{name} built rows")
+        check_rows(got, p.x_ctx[pick], W["W_DKV"], W["W_KR"], pos, d.rope_base, f"{name} built rows")
