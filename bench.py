@@ -489,7 +489,8 @@ def prefill_algorithmic(c: I.PrefillCase) -> dict:
     H, L, T = d.n_heads, c.prompt, c.queries
     pairs = sum(L - T + j + 1 for j in range(T))
     flops = 2.0 * L * d.d_c * H * (d.qk_nope + d.v_head) + 2.0 * pairs * H * (d.qk_nope + d.d_rope + d.v_head)
-    nbytes = 2.0 * (L * d.row + H * (d.qk_nope + d.v_head) * d.d_c + T * H * (d.qk_nope + d.d_rope) + T * H * d.v_head)
+    row = d.d_c + (H if c.rope_per_head else 1) * d.d_rope
+    nbytes = 2.0 * (L * row + H * (d.qk_nope + d.v_head) * d.d_c + T * H * (d.qk_nope + d.d_rope) + T * H * d.v_head)
     return {"flops": flops, "bytes": nbytes, "pairs": pairs}
 
 
@@ -550,7 +551,7 @@ def main():
     ap.add_argument("--sweep-reps", type=int, default=50)
     ap.add_argument("--prefill", action="store_true",
                     help="instead of the step benchmark, one JSON line per prefill case (explicit-form attention)")
-    ap.add_argument("--prefill-cases", default="prefill_dsv2_L4096_T4096,prefill_dsv2_L8192_T8192")
+    ap.add_argument("--prefill-cases", default="prefill_dsv2_L4096_T4096,prefill_dsv2_L8192_T8192,prefill_dsv2_L4096_T4096_rh")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -88,6 +88,7 @@ typedef struct {
   float softmax_scale;
   int dtype;           /* mla_dtype */
   int cache_fp8;       /* 0: cache rows in dtype; 1: reduced-precision cache (bf16 only, see below) */
+  int rope_per_head;   /* 0: one positional key per token shared by all heads; 1: one per head (below) */
 } mla_config;
 
 /* Paged latent cache.  Each token's row is [c_KV || k_R], d_c + d_rope values
@@ -100,6 +101,16 @@ typedef struct {
  *   token at pool[(k * (d_c + d_rope) + e) * block_size + o].
  * (Element-major blocks let the decode kernel fetch whole contiguous runs of a
  * block per copy and feed them to the tensor cores as either operand layout.)
+ *
+ * Per-head positional keys (rope_per_head = 1, dtype bf16, cache_fp8 = 0; [ZQ]
+ * "a small per-head RoPE-carrying key", the alternative to the shared key of
+ * [TM]/[SC]): a token's row is [c_KV (d_c) || k_R^1 (d_rope) || ... || k_R^H],
+ * row width d_c + n_heads * d_rope, each k_R^h = RoPE(W_KR^h x, pos) with the
+ * rotation frequencies restarting for every head; W_KR is then
+ * [n_heads * d_rope][d_model].  Supported by mla_compress_append and the
+ * explicit form (mla_prefill_attention); mla_decode_attention returns
+ * MLA_ERR_UNSUPPORTED (the absorbed kernel shares one key across heads as an
+ * MMA operand; per-head keys are a per-head dot product, not an MMA).
  *
  * Reduced-precision cache (cache_fp8 = 1, dtype bf16; [KJ "Compression as
  * architecture versus compression as post-processing"]: a latent can itself be
@@ -127,7 +138,8 @@ typedef struct {
 } mla_rope_table;
 
 /* Bytes one token occupies in the cache: (d_c + d_rope) * sizeof(dtype), or
- * d_c + 2 d_rope + 4 for the reduced-precision cache (644 at the DeepSeek-V2 shape).
+ * d_c + 2 d_rope + 4 for the reduced-precision cache (644 at the DeepSeek-V2 shape),
+ * or (d_c + n_heads * d_rope) * 2 with per-head positional keys.
  * [TM "Key Problems Solved"]: the per-token cache shrinks from 2*H*d to the
  * latent; [SC]: plus the positional part.  Returns 0 for an invalid config. */
 size_t mla_cache_bytes_per_token(const mla_config* cfg);

@@ -212,13 +212,14 @@ class PrefillLayer:
         c, d = p.case, p.dims
         self.device = device
         self.dt = tdtype(c.dtype)
-        self.cfg = M.make_config(d, c.dtype, cache_fp8=c.cache_fp8)
+        self.cfg = M.make_config(d, c.dtype, cache_fp8=c.cache_fp8, rope_per_head=c.rope_per_head)
         self.W = {k: to_dev(v, c.dtype, device) for k, v in p.weights.items()}
+        row = d.d_c + (d.n_heads if c.rope_per_head else 1) * d.d_rope
         if c.cache_fp8:
             self.pool = torch.full((p.num_blocks, d.block_size * (d.d_c + 2 * d.d_rope + 4)), 255, dtype=torch.uint8,
                                    device=device)
         else:
-            self.pool = torch.full((p.num_blocks, d.row, d.block_size), float("nan"), dtype=self.dt, device=device)
+            self.pool = torch.full((p.num_blocks, row, d.block_size), float("nan"), dtype=self.dt, device=device)
         self.block_table = torch.from_numpy(p.block_table).to(device)
         self.cache = M.make_cache(self.pool, self.block_table, d.block_size)
         max_pos = int(p.block_table.shape[1]) * d.block_size + 8

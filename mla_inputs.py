@@ -268,6 +268,7 @@ class PrefillCase:
     seq: int = 1
     note: str = ""
     cache_fp8: bool = False   # reduced-precision cache (fill "append" only)
+    rope_per_head: bool = False   # one positional key per head (row d_c + H d_rope; W_KR [H d_rope][d_model])
 
 
 PREFILL_CASES = {
@@ -286,6 +287,12 @@ PREFILL_CASES = {
         PrefillCase("prefill_dsv2_L8192_T8192", DSV2, "bf16", 8192, 8192, 47, note="an 8192-token prompt"),
         PrefillCase("prefill_dsv2_L333_T200_x_fp8", DSV2, "bf16", 333, 200, 48, fill="append", cache_fp8=True,
                     note="from hidden states over a reduced-precision cache"),
+        PrefillCase("prefill_dsv2_L300_T300_rh", DSV2, "bf16", 300, 300, 49, rope_per_head=True,
+                    note="per-head positional keys, drawn rows"),
+        PrefillCase("prefill_dsv2_L333_T333_x_rh", DSV2, "bf16", 333, 333, 50, fill="append", rope_per_head=True,
+                    note="per-head positional keys, from hidden states"),
+        PrefillCase("prefill_dsv2_L4096_T4096_rh", DSV2, "bf16", 4096, 4096, 51, rope_per_head=True,
+                    note="per-head positional keys, 4096-token prompt"),
     ]
 }
 
@@ -317,11 +324,15 @@ def make_prefill(c: PrefillCase, sharp: float = 1.0) -> PrefillProblem:
     rng = np.random.default_rng(c.seed)
     d = c.dims
     weights = draw_weights(d, c.dtype, rng)
+    row = d.d_c + (d.n_heads if c.rope_per_head else 1) * d.d_rope
+    if c.rope_per_head:
+        # one positional-key projection per head, drawn after the shared-key weights
+        weights["W_KR"] = storage(_normal(rng, (d.n_heads * d.d_rope, d.d_model), 1.0 / np.sqrt(d.d_model)), c.dtype)
     x = rows = q = None
     if c.fill == "append":
         x = draw_hidden(rng, c.prompt, d.d_model, c.dtype)
     else:
-        rows = storage(_normal(rng, (c.prompt, d.row), 1.0), c.dtype)
+        rows = storage(_normal(rng, (c.prompt, row), 1.0), c.dtype)
         qq = _normal(rng, (c.queries, d.n_heads, d.qk_nope + d.d_rope), 1.0)
         if sharp != 1.0:
             qq *= np.float32(sharp)

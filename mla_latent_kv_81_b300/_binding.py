@@ -29,7 +29,7 @@ class mla_config(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int), ("n_heads", ctypes.c_int), ("qk_nope", ctypes.c_int),
                 ("d_rope", ctypes.c_int), ("v_head", ctypes.c_int), ("d_c", ctypes.c_int),
                 ("block_size", ctypes.c_int), ("softmax_scale", ctypes.c_float), ("dtype", ctypes.c_int),
-                ("cache_fp8", ctypes.c_int)]
+                ("cache_fp8", ctypes.c_int), ("rope_per_head", ctypes.c_int)]
 
 
 class mla_paged_cache(ctypes.Structure):
@@ -88,9 +88,11 @@ EXPORTED = ("mla_cache_bytes_per_token", "mla_rope_table_create", "mla_compress_
 
 
 # ------------------------------------------------------------------ marshalling helpers
-def make_config(dims, dtype: str, softmax_scale: float = 0.0, cache_fp8: bool = False) -> mla_config:
+def make_config(dims, dtype: str, softmax_scale: float = 0.0, cache_fp8: bool = False,
+                rope_per_head: bool = False) -> mla_config:
     return mla_config(dims.d_model, dims.n_heads, dims.qk_nope, dims.d_rope, dims.v_head, dims.d_c,
-                      dims.block_size, softmax_scale, MLA_BF16 if dtype == "bf16" else MLA_F32, int(cache_fp8))
+                      dims.block_size, softmax_scale, MLA_BF16 if dtype == "bf16" else MLA_F32, int(cache_fp8),
+                      int(rope_per_head))
 
 
 def _ptr(t):

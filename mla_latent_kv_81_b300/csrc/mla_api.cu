@@ -88,6 +88,8 @@ mla_status check_cfg(const mla_config* c) {
   if (c->dtype != MLA_F32 && c->dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
   if (c->cache_fp8 != 0 && c->cache_fp8 != 1) return MLA_ERR_INVALID_ARG;
   if (c->cache_fp8 && c->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  if (c->rope_per_head != 0 && c->rope_per_head != 1) return MLA_ERR_INVALID_ARG;
+  if (c->rope_per_head && (c->dtype != MLA_BF16 || c->cache_fp8)) return MLA_ERR_UNSUPPORTED;
   if (c->d_rope % 2) return MLA_ERR_UNSUPPORTED;
   if (c->d_c > 512 || c->d_c + c->d_rope > 2048) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
@@ -246,6 +248,7 @@ const char* mla_status_string(mla_status s) {
 size_t mla_cache_bytes_per_token(const mla_config* cfg) {
   if (check_cfg(cfg) != MLA_OK) return 0;
   if (cfg->cache_fp8) return (size_t)cfg->d_c + 2 * (size_t)cfg->d_rope + 4;
+  if (cfg->rope_per_head) return ((size_t)cfg->d_c + (size_t)cfg->n_heads * cfg->d_rope) * 2;
   return (size_t)(cfg->d_c + cfg->d_rope) * elem_size(cfg->dtype);
 }
 

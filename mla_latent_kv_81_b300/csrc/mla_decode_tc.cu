@@ -975,8 +975,9 @@ WsLayout ws_layout(int items, int C) {
 }  // namespace
 
 bool tc_decode_supported(const mla_config* cfg, int batch, int n_q) {
-  return cfg->dtype == MLA_BF16 && cfg->n_heads == kH && cfg->d_c == kDC && cfg->d_rope == kDR &&
-         cfg->block_size == kBlk && batch > 0 && n_q > 0 && (long long)batch * n_q < (1LL << 24);
+  // one positional key shared by all heads: it is the B operand of the positional K-steps
+  return cfg->dtype == MLA_BF16 && !cfg->rope_per_head && cfg->n_heads == kH && cfg->d_c == kDC &&
+         cfg->d_rope == kDR && cfg->block_size == kBlk && batch > 0 && n_q > 0 && (long long)batch * n_q < (1LL << 24);
 }
 
 size_t tc_decode_workspace_bytes(const mla_config* cfg, int batch, int n_q, int max_blocks, int sm_count) {

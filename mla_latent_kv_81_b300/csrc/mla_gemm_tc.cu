@@ -328,6 +328,7 @@ __global__ void query_reduce_kernel(const float* part, int splits, int N, int H,
 constexpr int kAppTok = 8, kAppCols = 64;
 
 __global__ void __launch_bounds__(256) compress_reduce_kernel(const float* part, int splits, int T, int d_c, int d_r,
+                                                              int d_rh,
                                                               const int32_t* seq_idx, const int32_t* pos,
                                                               const float* rope, int rope_max, bf16* pool,
                                                               int num_blocks, const int32_t* table, int max_blocks,
@@ -374,7 +375,8 @@ __global__ void __launch_bounds__(256) compress_reduce_kernel(const float* part,
     }
     float2 v = make_float2((acc[0].x + acc[1].x) + (acc[2].x + acc[3].x), (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y));
     if (col >= d_c) {
-      const float* cs = rope + ((long long)p_t * (d_r / 2) + (col - d_c) / 2) * 2;
+      // rotation frequencies restart in every head's key when the keys are per head (d_rh < d_r)
+      const float* cs = rope + ((long long)p_t * (d_rh / 2) + ((col - d_c) % d_rh) / 2) * 2;
       float o0, o1;
       rope2(v.x, v.y, cs, o0, o1);
       v = make_float2(o0, o1);
@@ -549,13 +551,15 @@ bool tc_compress_supported(const mla_config* cfg, int T) {
 
 size_t tc_compress_workspace_bytes(const mla_config* cfg, int T, int sm_count) {
   if (!tc_compress_supported(cfg, T)) return 0;
-  return align256(partial_bytes(plan_stacked(cfg->d_c, cfg->d_rope, T, cfg->d_model, sm_count)));
+  const int d_r = cfg->rope_per_head ? cfg->n_heads * cfg->d_rope : cfg->d_rope;
+  return align256(partial_bytes(plan_stacked(cfg->d_c, d_r, T, cfg->d_model, sm_count)));
 }
 
 cudaError_t tc_compress_append(const Ctx& ctx, const mla_config* cfg, const void* x, const void* W_DKV,
                                const void* W_KR, const int32_t* seq_idx, const int32_t* pos,
                                const mla_rope_table& rope, const mla_paged_cache& cache, int T, void* workspace) {
-  const int D = cfg->d_model, d_c = cfg->d_c, d_r = cfg->d_rope;
+  const int D = cfg->d_model, d_c = cfg->d_c, d_rh = cfg->d_rope;
+  const int d_r = cfg->rope_per_head ? cfg->n_heads * d_rh : d_rh;   // positional columns of a row
   GemmPlan pl = plan_stacked(d_c, d_r, T, D, ctx.sm_count);
   pl.args.partial = static_cast<float*>(workspace);
   CUtensorMap a1, a2, b;
@@ -570,7 +574,7 @@ cudaError_t tc_compress_append(const Ctx& ctx, const mla_config* cfg, const void
                                       cfg->block_size);
   const int width = d_c + d_r;
   dim3 grid((T + kAppTok - 1) / kAppTok, (width + kAppCols - 1) / kAppCols);
-  compress_reduce_kernel<<<grid, 256, 0, ctx.stream>>>(pl.args.partial, pl.args.splits, T, d_c, d_r, seq_idx, pos,
+  compress_reduce_kernel<<<grid, 256, 0, ctx.stream>>>(pl.args.partial, pl.args.splits, T, d_c, d_r, d_rh, seq_idx, pos,
                                                        rope.cos_sin, rope.max_pos, (bf16*)cache.pool,
                                                        cache.num_blocks, cache.block_table, cache.max_blocks_per_seq,
                                                        cache.batch, cfg->block_size, ctx.status);

@@ -8,7 +8,8 @@
 // this form costs 2 (qk_nope + d_rope + v_head) FLOP per (query, key, head), against
 // 2 (d_c + d_rope + d_c) for the absorbed form, so the keys and values are rebuilt once:
 //   1. gather_latent_kernel: the sequence's rows, stored element-major per cache block, into one
-//      chunk-major buffer lat[(d_c + d_rope) / 64][L][64];
+//      chunk-major buffer lat[row / 64][L][64] (row = d_c + d_rope, or d_c + H d_rope with per-head
+//      positional keys, head h's key then in chunk d_c / 64 + h);
 //   2. tc_reconstruct_kv (projection GEMM): per-head keys W_UK^h c_t and values W_UV^h c_t, chunk-major
 //      kv[4H][L][64] (64-element chunk 2h + c of head h's key, 2H + 2h + c of its value);
 //   Every TMA box of the GEMM and of the attention kernel over these buffers is one contiguous run
@@ -73,6 +74,7 @@ static_assert(sizeof(FCtrl) <= kOffKRing, "control block");
 struct FParams {
   int T, L, q0;       // queries, keys (cached prompt rows), position of query 0 (= L - T)
   int H, qtiles, units;
+  int rope_chunk, rope_step;   // chunk of lat holding head h's positional key: rope_chunk + h * rope_step
   float scale_log2;
   bf16* o;            // [T][H][v_head]
   float* lse;         // [T][H] or null
@@ -103,8 +105,8 @@ __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
 // (64-token cache block, 64-element chunk): the block's element rows (64 tokens, contiguous) are read,
 // transposed through shared memory and written as 64 rows of 128 B (one contiguous 8 KB run).
 // Out-of-range block-table entries flag an index error and give zero rows.
-__global__ void __launch_bounds__(256) gather_latent_kernel(const bf16* pool, const int32_t* table, int max_blocks,
-                                                            int num_blocks, int seq, int L, bf16* lat,
+__global__ void __launch_bounds__(256) gather_latent_kernel(const bf16* pool, int row_w, const int32_t* table,
+                                                            int max_blocks, int num_blocks, int seq, int L, bf16* lat,
                                                             uint32_t* status) {
   __shared__ uint16_t tile[64][65];
   const int bt = blockIdx.x, e0 = blockIdx.y * 64;
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(256) gather_latent_kernel(const bf16* pool, co
   const uint16_t* src = reinterpret_cast<const uint16_t*>(pool);
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
     const int e = i >> 6, t = i & 63;
-    tile[e][t] = blk >= 0 ? src[((long long)blk * kRowW + e0 + e) * kFBlk + t] : (uint16_t)0;
+    tile[e][t] = blk >= 0 ? src[((long long)blk * row_w + e0 + e) * kFBlk + t] : (uint16_t)0;
   }
   __syncthreads();
   uint16_t* dst = reinterpret_cast<uint16_t*>(lat);
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           if (!load_chunk(&mapq, c * 64, h, qt * kFT)) goto done;
         for (int j = 0; j < n; ++j)
           if (!load_chunk(&mapkv, 0, j * kFT, 2 * h) || !load_chunk(&mapkv, 0, j * kFT, 2 * h + 1) ||
-              !load_chunk(&mapr, 0, j * kFT, kDC / 64))
+              !load_chunk(&mapr, 0, j * kFT, p.rope_chunk + h * p.rope_step))
             goto done;
       }
     }
@@ -431,11 +433,14 @@ done:
 struct PrefillLayout {
   size_t lat, kv, total;
 };
-PrefillLayout prefill_layout(int L) {
+// Width of a cache row: the latent and one positional key, or one positional key per head.
+int row_width(const mla_config* cfg) { return cfg->d_c + (cfg->rope_per_head ? cfg->n_heads : 1) * cfg->d_rope; }
+
+PrefillLayout prefill_layout(int L, int row_w) {
   PrefillLayout w;
   auto a256 = [](size_t v) { return (v + 255) / 256 * 256; };
   w.lat = 0;
-  w.kv = a256((size_t)L * kRowW * 2);
+  w.kv = a256((size_t)L * row_w * 2);
   w.total = w.kv + a256((size_t)L * 2 * kH * kQK * 2);
   return w;
 }
@@ -449,14 +454,14 @@ bool tc_prefill_supported(const mla_config* cfg) {
 
 size_t tc_prefill_workspace_bytes(const mla_config* cfg, int kv_len) {
   if (!tc_prefill_supported(cfg) || kv_len <= 0) return 0;
-  return prefill_layout(kv_len).total;
+  return prefill_layout(kv_len, row_width(cfg)).total;
 }
 
 cudaError_t tc_prefill_attention(const Ctx& ctx, const mla_config* cfg, const void* q, const mla_paged_cache& cache,
                                  int seq, int kv_len, int T, const void* W_UK, const void* W_UV, float scale, void* o,
                                  float* lse, void* workspace) {
-  const int L = kv_len, H = kH;
-  const PrefillLayout w = prefill_layout(L);
+  const int L = kv_len, H = kH, row_w = row_width(cfg);
+  const PrefillLayout w = prefill_layout(L, row_w);
   char* base = static_cast<char*>(workspace);
   bf16* lat = reinterpret_cast<bf16*>(base + w.lat);
   bf16* kv = reinterpret_cast<bf16*>(base + w.kv);
@@ -464,8 +469,8 @@ cudaError_t tc_prefill_attention(const Ctx& ctx, const mla_config* cfg, const vo
   if (cfg->cache_fp8) {
     e = launch_gather_latent_fp8(ctx, cfg, cache, seq, L, lat);
   } else {
-    const dim3 gg((L + kFBlk - 1) / kFBlk, kRowW / 64);
-    gather_latent_kernel<<<gg, 256, 0, ctx.stream>>>(static_cast<const bf16*>(cache.pool), cache.block_table,
+    const dim3 gg((L + kFBlk - 1) / kFBlk, row_w / 64);
+    gather_latent_kernel<<<gg, 256, 0, ctx.stream>>>(static_cast<const bf16*>(cache.pool), row_w, cache.block_table,
                                                      cache.max_blocks_per_seq, cache.num_blocks, seq, L, lat,
                                                      ctx.status);
     count_launch();
@@ -477,7 +482,7 @@ cudaError_t tc_prefill_attention(const Ctx& ctx, const mla_config* cfg, const vo
   CUtensorMap mapq, mapkv, mapr;
   const uint64_t dq[3] = {(uint64_t)kQW, (uint64_t)H, (uint64_t)T}, sq[2] = {(uint64_t)kQW * 2, (uint64_t)H * kQW * 2};
   const uint64_t dkv[3] = {64, (uint64_t)L, (uint64_t)4 * H}, skv[2] = {128, (uint64_t)L * 128};
-  const uint64_t dr[3] = {64, (uint64_t)L, (uint64_t)kRowW / 64}, sr[2] = {128, (uint64_t)L * 128};
+  const uint64_t dr[3] = {64, (uint64_t)L, (uint64_t)row_w / 64}, sr[2] = {128, (uint64_t)L * 128};
   const uint32_t boxq[3] = {64, 1, kFT}, boxc[3] = {64, kFT, 1};
   if (!encode_map_bf16(&mapq, q, 3, dq, sq, boxq) || !encode_map_bf16(&mapkv, kv, 3, dkv, skv, boxc) ||
       !encode_map_bf16(&mapr, lat, 3, dr, sr, boxc))
@@ -489,6 +494,8 @@ cudaError_t tc_prefill_attention(const Ctx& ctx, const mla_config* cfg, const vo
   fp.H = H;
   fp.qtiles = (T + kFT - 1) / kFT;
   fp.units = H * fp.qtiles;
+  fp.rope_chunk = kDC / 64;
+  fp.rope_step = cfg->rope_per_head ? kDR / 64 : 0;
   fp.scale_log2 = scale * kLog2e;
   fp.o = static_cast<bf16*>(o);
   fp.lse = lse;

@@ -115,6 +115,19 @@ def compress(x, W_DKV, W_KR, pos, base: float = 10000.0):
     return c, k_r
 
 
+def compress_per_head_rope(x, W_DKV, W_KR, pos, n_heads: int, base: float = 10000.0):
+    """The per-head positional-key variant ([ZQ] "a small per-head RoPE-carrying key"; the alternative
+    to reading c1): k_R^h,t = RoPE(W_KR^h x_t, pos_t) for every head, W_KR stored [n_heads * d_rope]
+    [d_model] (head h's rows h*d_rope .. h*d_rope + d_rope - 1), the rotation frequencies restarting in
+    every head's key.  Returns (c [T, d_c], k_R [T, n_heads, d_rope])."""
+    x = _a(x)
+    c = x @ _a(W_DKV).T
+    y = x @ _a(W_KR).T
+    y = y.reshape(x.shape[0], n_heads, -1)
+    k_r = apply_rope(y, _a(pos)[:, None], base)
+    return c, k_r
+
+
 def project_query(x, W_Q, W_QR, q_pos, n_heads: int, base: float = 10000.0):
     """Per-head content query q_nope^h = W_Q^h x and rotated query q_R^h = RoPE(W_QR^h x, q_pos).
 
@@ -170,7 +183,8 @@ def attend_explicit(q_nope, q_rope, c, k_r, W_UK, W_UV, kv_len: int, scale: floa
     [KJ §The mechanism, solid answer]; [BB §1 eq., §2, Implementation Logic
     step 5: content and positional key combined, reading c2]; [SC] every prior
     token keeps an entry (no token selection).
-    q_nope [n_q, H, qk_nope], q_rope [n_q, H, d_rope], c [L, d_c], k_r [L, d_rope].
+    q_nope [n_q, H, qk_nope], q_rope [n_q, H, d_rope], c [L, d_c], k_r [L, d_rope], or [L, H, d_rope]
+    with a positional key per head (head h scores q_R^h against its own k_R^h).
     Returns o [n_q, H, v_head].
     """
     q_nope, q_rope, c, k_r = _a(q_nope), _a(q_rope), _a(c), _a(k_r)
@@ -185,7 +199,8 @@ def attend_explicit(q_nope, q_rope, c, k_r, W_UK, W_UV, kv_len: int, scale: floa
             vis = visible(kv_len, n_q, j)
             if vis == 0:
                 continue                                   # reading c10
-            s = scale * (K_h[:vis] @ q_nope[j, h] + k_r[:vis] @ q_rope[j, h])
+            kr = k_r[:vis, h] if k_r.ndim == 3 else k_r[:vis]
+            s = scale * (K_h[:vis] @ q_nope[j, h] + kr @ q_rope[j, h])
             p, _ = _softmax_weights(s)
             out[j, h] = p @ V_h[:vis]
     return out
@@ -220,7 +235,8 @@ def attend_explicit_at(q_nope, q_rope, pos, c, k_r, W_UK, W_UV, scale: float, st
             K_h, V_h = store(K_h), store(V_h)
         for j in range(n):
             vis = int(pos[j]) + 1
-            s = scale * (K_h[:vis] @ q_nope[j, h] + k_r[:vis] @ q_rope[j, h])
+            kr = k_r[:vis, h] if k_r.ndim == 3 else k_r[:vis]
+            s = scale * (K_h[:vis] @ q_nope[j, h] + kr @ q_rope[j, h])
             p, lse[j, h] = _softmax_weights(s)
             o[j, h] = p @ V_h[:vis]
     return o, lse

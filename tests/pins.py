@@ -171,6 +171,41 @@ def check_sdpa(seed, d_model, H, qk_nope, d_rope, v_head, d_c, L, n_q, tol=1e-12
     assert err <= tol, err
 
 
+def check_per_head_rope(seed=13, d_model=48, H=3, qk_nope=5, d_rope=4, v_head=6, d_c=7, L=11):
+    """The per-head positional keys: with every head's W_KR^h equal to one W_KR the keys and the result
+    equal the shared-key ones; with different heads, torch's scaled_dot_product_attention (float64) over
+    K^h = [W_UK^h c || k_R^h] agrees with attend_explicit_at; the rotation restarts per head (head h's
+    key equals the shared rotation of its own rows)."""
+    import torch
+    pos = np.arange(L - 4, L)
+    W, x_ctx, x_q = small_problem(seed, d_model, H, qk_nope, d_rope, v_head, d_c, L, len(pos), sharp=2.0)
+    W_KR_h = np.random.default_rng(seed + 1).standard_normal((H * d_rope, d_model)) / math.sqrt(d_model)
+    c1, k1 = O.compress(x_ctx, W["W_DKV"], W["W_KR"], np.arange(L))
+    c2, k2 = O.compress_per_head_rope(x_ctx, W["W_DKV"], np.tile(W["W_KR"], (H, 1)), np.arange(L), H)
+    assert np.allclose(c1, c2) and all(np.allclose(k2[:, h], k1, atol=1e-13) for h in range(H))
+    for h in range(H):
+        _, kh = O.compress(x_ctx, W["W_DKV"], W_KR_h[h * d_rope:(h + 1) * d_rope], np.arange(L))
+        _, kall = O.compress_per_head_rope(x_ctx, W["W_DKV"], W_KR_h, np.arange(L), H)
+        assert np.allclose(kall[:, h], kh, atol=1e-13)
+    q_nope, q_rope = O.project_query(x_q, W["W_Q"], W["W_QR"], pos, H)
+    scale = O.softmax_scale(qk_nope, d_rope)
+    s1, _ = O.attend_explicit_at(q_nope, q_rope, pos, c1, k1, W["W_UK"], W["W_UV"], scale)
+    s2, _ = O.attend_explicit_at(q_nope, q_rope, pos, c2, k2, W["W_UK"], W["W_UV"], scale)
+    assert np.max(np.abs(s1 - s2)) <= 1e-12
+    _, kall = O.compress_per_head_rope(x_ctx, W["W_DKV"], W_KR_h, np.arange(L), H)
+    got, _ = O.attend_explicit_at(q_nope, q_rope, pos, c1, kall, W["W_UK"], W["W_UV"], scale)
+    K = np.stack([np.concatenate([O.reconstruct_kv(c1, W["W_UK"], W["W_UV"], h)[0], kall[:, h]], axis=1) for h in range(H)])
+    V = np.stack([O.reconstruct_kv(c1, W["W_UK"], W["W_UV"], h)[1] for h in range(H)])
+    Q = np.concatenate([q_nope, q_rope], axis=2).transpose(1, 0, 2)
+    mask = np.arange(L)[None, :] <= pos[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+        attn_mask=torch.from_numpy(mask), scale=scale)[0].numpy().transpose(1, 0, 2)
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= 1e-12
+    out_e = O.attend_explicit(q_nope, q_rope, c1, kall, W["W_UK"], W["W_UV"], L, scale)
+    assert np.max(np.abs(out_e - got)) <= 1e-12
+
+
 def check_prefill_rows(seed, d_model, H, qk_nope, d_rope, v_head, d_c, L, pos, tol=1e-12):
     """attend_explicit_at against torch's scaled_dot_product_attention (CPU, float64) with the
     prompt's causal mask over the rebuilt K and V; its lse against the absorbed form's (the pages'

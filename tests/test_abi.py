@@ -47,6 +47,11 @@ def test_cache_bytes_per_token_matches_closed_form():
     bad = M.make_config(I.DSV2, "bf16")
     bad.cache_fp8 = 2
     assert M.mla_cache_bytes_per_token(bad) == 0
+    # per-head positional keys: the row holds the latent and one key per head
+    rh = M.make_config(I.DSV2, "bf16", rope_per_head=True)
+    assert M.mla_cache_bytes_per_token(rh) == (512 + 128 * 64) * 2
+    assert M.mla_decode_workspace_bytes(rh, 2, 1, 4) == 0          # absorbed decode: one shared key only
+    assert M.mla_prefill_workspace_bytes(rh, 100) > M.mla_prefill_workspace_bytes(M.make_config(I.DSV2, "bf16"), 100)
     # the decode workspace of a reduced-precision cache also holds the expanded bf16 blocks
     f8 = M.make_config(I.DSV2, "bf16", cache_fp8=True)
     assert M.mla_decode_workspace_bytes(f8, 4, 1, 10) >= M.mla_decode_workspace_bytes(cfg := M.make_config(I.DSV2, "bf16"), 4, 1, 10) + 40 * 576 * 64 * 2

@@ -48,6 +48,10 @@ def test_prefill_rows_against_sdpa(shape):
     pins.check_prefill_rows(seed=6, **shape)
 
 
+def test_per_head_rope_keys():
+    pins.check_per_head_rope()
+
+
 def test_fp8_cache_format():
     pins.check_fp8_format()
 

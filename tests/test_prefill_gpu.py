@@ -25,7 +25,7 @@ from oracle import mla_oracle as O
 pytestmark = pytest.mark.gpu
 
 SMALL = ["prefill_dsv2_L300_T300", "prefill_dsv2_L700_T200", "prefill_dsv2_L300_T1", "prefill_dsv2_L64_T64",
-         "prefill_dsv2_L1_T1"]
+         "prefill_dsv2_L1_T1", "prefill_dsv2_L300_T300_rh"]
 LSE_TOL = 2e-2
 
 
@@ -34,7 +34,8 @@ def oracle_rows(p: I.PrefillProblem, idx=None):
     pos = p.q_pos if idx is None else p.q_pos[idx]
     q = (p.q if idx is None else p.q[idx]).astype(np.float64)
     rows = p.rows.astype(np.float64)
-    return O.attend_explicit_at(q[..., :d.qk_nope], q[..., d.qk_nope:], pos, rows[:, :d.d_c], rows[:, d.d_c:],
+    k_r = rows[:, d.d_c:].reshape(rows.shape[0], d.n_heads, d.d_rope) if p.case.rope_per_head else rows[:, d.d_c:]
+    return O.attend_explicit_at(q[..., :d.qk_nope], q[..., d.qk_nope:], pos, rows[:, :d.d_c], k_r,
                                 W["W_UK"], W["W_UV"], O.softmax_scale(d.qk_nope, d.d_rope), store=O.round_bf16)
 
 
@@ -58,8 +59,9 @@ def test_prefill_attention_matches_the_explicit_oracle(name, sharp):
     assert np.max(np.abs(lse - ref_lse)) <= LSE_TOL, f"{name} x{sharp:g} lse"
 
 
-def test_prefill_from_hidden_states_matches_the_float64_chain():
-    c = I.PREFILL_CASES["prefill_dsv2_L333_T333_x"]
+@pytest.mark.parametrize("name", ["prefill_dsv2_L333_T333_x", "prefill_dsv2_L333_T333_x_rh"])
+def test_prefill_from_hidden_states_matches_the_float64_chain(name):
+    c = I.PREFILL_CASES[name]
     p = I.make_prefill(c)
     d, W = p.dims, p.weights
     L = Hn.PrefillLayer(p)
@@ -75,7 +77,10 @@ def test_prefill_from_hidden_states_matches_the_float64_chain():
     assert_close_rows(q[..., :d.qk_nope], q_nope, "q_nope")
     assert_close_rows(q[..., d.qk_nope:], q_rope, "q_rope")
     # the layer output against the pure float64 explicit chain from the hidden states
-    cc, k_r = O.compress(p.x, W["W_DKV"], W["W_KR"], np.arange(c.prompt), d.rope_base)
+    if c.rope_per_head:
+        cc, k_r = O.compress_per_head_rope(p.x, W["W_DKV"], W["W_KR"], np.arange(c.prompt), d.n_heads, d.rope_base)
+    else:
+        cc, k_r = O.compress(p.x, W["W_DKV"], W["W_KR"], np.arange(c.prompt), d.rope_base)
     ref = O.decode_layer_explicit(xq, p.q_pos, [(cc, k_r)], W, d, c.queries, [c.prompt])
     assert_close_rows(L.out.float().cpu().numpy(), ref, "out")
 
@@ -111,3 +116,16 @@ def test_prefill_bad_block_entry_is_flagged_not_faulted():
     code, flags = L.status()
     assert code == 5 and flags & 1
     assert np.all(np.isfinite(L.o.float().cpu().numpy()))
+
+
+def test_per_head_keys_are_refused_by_the_absorbed_decode():
+    """The absorbed decode kernel shares one positional key across heads (an MMA operand); with per-head
+    keys mla_decode_attention returns MLA_ERR_UNSUPPORTED and its workspace size is 0."""
+    import ctypes
+    import mla_latent_kv_81_b300 as M
+    cfg = M.make_config(I.DSV2, "bf16", rope_per_head=True)
+    assert M.mla_decode_workspace_bytes(cfg, 2, 1, 4) == 0
+    cache = M.mla_paged_cache(0x2000, 8, 0x3000, 4, 2)
+    fake = lambda n: ctypes.c_void_p(0x10000 * n)
+    assert M.lib.mla_decode_attention(ctypes.byref(cfg), fake(1), ctypes.byref(cache), fake(2), 2, 1, fake(3), None,
+                                      fake(4), 1 << 30, None) == 2
