@@ -24,6 +24,8 @@ def to_dev(a: np.ndarray, dtype: str, device="cuda"):
 class DeviceLayer:
     """One MLA layer's weights, paged cache and RoPE table on the device."""
 
+    fp8 = False   # reduced-precision cache (set per workload in __init__)
+
     def __init__(self, p: I.Problem, device="cuda", max_pos: int | None = None):
         self.p = p
         w, d = p.w, p.dims
