@@ -47,6 +47,15 @@ __device__ __forceinline__ int cache_block(const int32_t* table, int max_blocks,
   return (blk < 0 || blk >= num_blocks) ? -1 : blk;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Every kernel of the decode step lets the next kernel in its stream be scheduled as soon as it starts
+// (pdl_trigger), and reads or writes global memory only after the kernel before it has completed
+// (pdl_wait, placed after the CTA's own set-up: barrier init, TMEM allocation, tensor-map prefetch).
+// A kernel's set-up thus overlaps the previous kernel's tail; since every kernel waits before it
+// completes, completion stays ordered along the stream.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ launch plumbing
 struct Ctx {
   cudaStream_t stream;
@@ -64,6 +73,23 @@ mla_status validate_append(const mla_config* cfg, const void* x, const void* W_D
 size_t append_scratch_bytes(const mla_config* cfg, int T);
 // The append after validation: `scratch` holds append_scratch_bytes(cfg, T) bytes; device-side
 // flags go to the status word in the header of `status_ws`, or to the library's word when null.
+// Launch `kernel` as a programmatic dependent of the previous kernel in `stream` (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, static_cast<KArgs>(args)...);
+}
+
 mla_status run_append(const mla_config* cfg, const void* x, const void* W_DKV, const void* W_KR,
                       const int32_t* seq_idx, const int32_t* pos, const mla_rope_table* rope,
                       const mla_paged_cache* cache, int T, void* scratch, void* status_ws, cudaStream_t stream);

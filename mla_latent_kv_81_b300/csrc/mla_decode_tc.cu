@@ -373,8 +373,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int cid = (int)cluster_id_x();
   volatile int* abort_flag = &ctrl->abort_flag;
 
-  // the merge kernel may be scheduled now; it waits for this grid to finish before reading anything
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the next kernel (the merge) may be scheduled now; it waits for this grid before touching memory
+  pdl_trigger();
   if (tid == 0) {
     for (int i = 0; i < kRing; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
@@ -402,6 +402,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefetch_tmap(&mapv);
     prefetch_tmap(&mapq);
   }
+  // everything below reads what earlier kernels of the stream wrote (queries, appended rows)
+  pdl_wait();
   if (warp == 3) plan_cluster(p, ctrl, cid, (int)num_clusters_x());
   tc_fence_before();
   __syncthreads();
@@ -861,7 +863,8 @@ constexpr int kMergeGroups = kDC / 16;
 
 __global__ void __launch_bounds__(kH) merge_kernel(const int* prefix, int items, int clusters, const __half* part_o,
                                                    const float* part_lse, bf16* o_lat, float* lse_out) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_trigger();
+  pdl_wait();
   const int item = blockIdx.x, g = blockIdx.y, h = threadIdx.x;
   const int T = prefix[items];
   const int P0 = prefix[item], P1 = prefix[item + 1];
@@ -1038,8 +1041,9 @@ cudaError_t tc_decode_attention(const Ctx& ctx, const mla_config* cfg, const voi
   prm.status = ctx.status;
   cudaError_t e = ensure_smem_limit((const void*)decode_tc_kernel, kSmemBytes, ctx.device);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<<<2 * C, kThreads, kSmemBytes, ctx.stream>>>(mapk, mapv, mapq, prm);
+  e = launch_pdl(decode_tc_kernel, dim3(2 * C), dim3(kThreads), kSmemBytes, ctx.stream, mapk, mapv, mapq, prm);
   count_launch();
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

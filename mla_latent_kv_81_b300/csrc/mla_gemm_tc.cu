@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   uint8_t* ring = smem + kGCtrl;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &ctrl->abort_flag;
+  pdl_trigger();
 
   if (tid == 0) {
     for (int i = 0; i < a.stages; ++i) { mbar_init(&ctrl->full[i], 1); mbar_init(&ctrl->empty[i], 1); }
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();
   const uint32_t tmem = ctrl->tmem_base;
   const uint32_t ring_base = smem_u32(ring);
   const uint32_t b_bytes = (uint32_t)a.n_tile * 128;
@@ -250,6 +252,8 @@ __device__ __forceinline__ float4 sum_splits4(const float* part, int splits, lon
 __global__ void absorb_reduce_kernel(const float* part, int splits, int N, int H, int qk, int d_r, int d_c,
                                      const int32_t* q_pos, const float* rope, int rope_max, bf16* q_nope,
                                      bf16* q_out, uint32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const int Mt = H * (qk + d_r);
   const long long total4 = (long long)N * Mt / 4, stride = (long long)N * Mt;
   for (long long e4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; e4 < total4;
@@ -290,6 +294,8 @@ __global__ void absorb_reduce_kernel(const float* part, int splits, int N, int H
 // One thread per 4 consecutive columns.
 __global__ void query_reduce_kernel(const float* part, int splits, int N, int H, int qk, int d_r, const int32_t* q_pos,
                                     const float* rope, int rope_max, bf16* q_out, uint32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const int Mt = H * (qk + d_r);
   const long long total4 = (long long)N * Mt / 4, stride = (long long)N * Mt;
   for (long long e4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; e4 < total4;
@@ -335,6 +341,8 @@ __global__ void __launch_bounds__(256) compress_reduce_kernel(const float* part,
                                                               int batch, int block_size, uint32_t* status) {
   __shared__ bf16 tile[kAppCols][kAppTok];
   __shared__ long long dst_base[kAppTok];   // pool offset of column 0 of each token, or -1 (skipped)
+  pdl_trigger();
+  pdl_wait();
   const int t0 = blockIdx.x * kAppTok, c0 = blockIdx.y * kAppCols;
   const int width = d_c + d_r;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -396,6 +404,8 @@ __global__ void __launch_bounds__(256) compress_reduce_kernel(const float* part,
 
 // bf16 output from k-split partials ([splits][count]), 4 elements per thread.
 __global__ void sum_to_bf16_kernel(const float* part, int splits, long long count, bf16* out) {
+  pdl_trigger();
+  pdl_wait();
   for (long long e4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; e4 < count / 4;
        e4 += (long long)gridDim.x * blockDim.x) {
     const float4 v = sum_splits4(part, splits, count, e4 * 4);
@@ -511,11 +521,13 @@ cudaError_t launch_gemm(const Ctx& ctx, const CUtensorMap& am, const CUtensorMap
   cudaError_t e = ensure_smem_limit(kern, kGSmem, ctx.device);
   if (e != cudaSuccess) return e;
   if (p.args.units == 0) return cudaSuccess;
+  e = cudaSuccess;
   if (p.args.a_mn)
-    gemm_tc_kernel<true><<<p.grid, kGThreads, kGSmem, ctx.stream>>>(am, am2, bm, p.args);
+    e = launch_pdl(gemm_tc_kernel<true>, dim3(p.grid), dim3(kGThreads), kGSmem, ctx.stream, am, am2, bm, p.args);
   else
-    gemm_tc_kernel<false><<<p.grid, kGThreads, kGSmem, ctx.stream>>>(am, am2, bm, p.args);
+    e = launch_pdl(gemm_tc_kernel<false>, dim3(p.grid), dim3(kGThreads), kGSmem, ctx.stream, am, am2, bm, p.args);
   count_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -574,11 +586,11 @@ cudaError_t tc_compress_append(const Ctx& ctx, const mla_config* cfg, const void
                                       cfg->block_size);
   const int width = d_c + d_r;
   dim3 grid((T + kAppTok - 1) / kAppTok, (width + kAppCols - 1) / kAppCols);
-  compress_reduce_kernel<<<grid, 256, 0, ctx.stream>>>(pl.args.partial, pl.args.splits, T, d_c, d_r, d_rh, seq_idx, pos,
-                                                       rope.cos_sin, rope.max_pos, (bf16*)cache.pool,
-                                                       cache.num_blocks, cache.block_table, cache.max_blocks_per_seq,
-                                                       cache.batch, cfg->block_size, ctx.status);
+  e = launch_pdl(compress_reduce_kernel, grid, dim3(256), 0, ctx.stream, pl.args.partial, pl.args.splits, T, d_c, d_r,
+                 d_rh, seq_idx, pos, rope.cos_sin, rope.max_pos, (bf16*)cache.pool, cache.num_blocks, cache.block_table,
+                 cache.max_blocks_per_seq, cache.batch, cfg->block_size, ctx.status);
   count_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -630,11 +642,11 @@ cudaError_t tc_absorb_query(const Ctx& ctx, const mla_config* cfg, const void* x
   cudaError_t e = launch_gemm(ctx, aq, ar, bx, l.pqr);
   if (e != cudaSuccess) return e;
   const long long work = (long long)N * H * (qk + d_r) / 4;
-  absorb_reduce_kernel<<<launch_blocks(work, 256, ctx.sm_count), 256, 0, ctx.stream>>>(
-      l.pqr.args.partial, l.pqr.args.splits, N, H, qk, d_r, d_c, q_pos, rope.cos_sin, rope.max_pos, q_nope,
-      (bf16*)q_out, ctx.status);
+  e = launch_pdl(absorb_reduce_kernel, dim3(launch_blocks(work, 256, ctx.sm_count)), dim3(256), 0, ctx.stream,
+                 l.pqr.args.partial, l.pqr.args.splits, N, H, qk, d_r, d_c, q_pos, rope.cos_sin, rope.max_pos, q_nope,
+                 (bf16*)q_out, ctx.status);
   count_launch();
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // q_abs^h = W_UK^h^T q_nope^h, written straight into q_out[n][h][0:d_c]
   l.pa.args.partial = nullptr;
@@ -693,9 +705,10 @@ cudaError_t tc_output_project(const Ctx& ctx, const mla_config* cfg, const void*
   e = launch_gemm(ctx, awo, awo, bo, l.po);
   if (e != cudaSuccess) return e;
   const long long count = (long long)N * D;
-  sum_to_bf16_kernel<<<launch_blocks(count / 4, 256, ctx.sm_count), 256, 0, ctx.stream>>>(
-      l.po.args.partial, l.po.args.splits, count, static_cast<bf16*>(out));
+  e = launch_pdl(sum_to_bf16_kernel, dim3(launch_blocks(count / 4, 256, ctx.sm_count)), dim3(256), 0, ctx.stream,
+                 l.po.args.partial, l.po.args.splits, count, static_cast<bf16*>(out));
   count_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
