@@ -266,6 +266,11 @@ def check_fp8_format(seed=12):
     assert np.all(np.abs(codes_v) <= 448)
     err = np.abs(codes_v * s[:, None] - rows)
     assert np.all(err <= 2.0 ** -4 * np.abs(rows) + 2.0 ** -10 * s[:, None])
+    # the stored positional key: (k_R / s) rounded to bf16, times s, is k_R within half a bf16 ulp
+    keys = rng.standard_normal((500, 16)) * 2.0 ** rng.uniform(-5, 5, (500, 1))
+    _, s2, krs = O.quantize_latent_fp8(rows, keys)
+    _, k_back = O.dequantize_latent_fp8(np.zeros_like(rows), s2, krs)
+    assert np.all(np.abs(k_back - keys) <= 2.0 ** -8 * np.abs(keys))
 
 
 def check_rope_properties(d_rope=16, base=10000.0):

@@ -71,6 +71,63 @@ def _compress_unrotated(x, W_DKV, W_KR, pos, base=10000.0):
     return ORIG["compress"](x, W_DKV, W_KR, np.zeros_like(np.asarray(pos)), base)
 
 
+def _prefill_window_off_by_one(q_nope, q_rope, pos, c, k_r, W_UK, W_UV, scale, store=None):
+    # each query sees positions 0..pos-1 instead of 0..pos (its own token left out)
+    pos = np.asarray(pos)
+    o, lse = ORIG["attend_explicit_at"](q_nope, q_rope, np.maximum(pos - 1, 0), c, k_r, W_UK, W_UV, scale, store)
+    return o, lse
+
+
+def _prefill_first_head_key(q_nope, q_rope, pos, c, k_r, W_UK, W_UV, scale, store=None):
+    # per-head keys read as one shared key (head 0's)
+    k_r = np.asarray(k_r)
+    if k_r.ndim == 3:
+        k_r = k_r[:, 0]
+    return ORIG["attend_explicit_at"](q_nope, q_rope, pos, c, k_r, W_UK, W_UV, scale, store)
+
+
+def _e4m3_ties_away(x):
+    x = np.asarray(x, dtype=float)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    q = 2.0 ** (np.maximum(e, -6.0) - 3.0)
+    return np.sign(x) * np.floor(a / q + 0.5) * q
+
+
+def _e4m3_no_subnormal_clamp(x):
+    x = np.asarray(x, dtype=float)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    q = 2.0 ** (e - 3.0)                 # keeps 3 mantissa bits below 2^-6 as well
+    return np.sign(x) * np.round(a / q) * q
+
+
+def _e4m3_value_bias8(code):
+    c = np.asarray(code, dtype=np.int64)
+    sgn = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -7, (1.0 + m / 8.0) * 2.0 ** (e - 8.0))
+    return np.where((c & 0x7F) == 0x7F, np.nan, sgn * val)
+
+
+def _scale_floor(c):
+    m = np.max(np.abs(np.asarray(c, dtype=float)), axis=-1)
+    return 2.0 ** np.floor(np.log2(np.where(m > 0, m, 448.0) / 448.0))
+
+
+def _per_head_rope_flat(x, W_DKV, W_KR, pos, n_heads, base=10000.0):
+    # one rotation over the whole H*d_rope row: frequencies do not restart in each head's key
+    x = np.asarray(x, dtype=float)
+    c = x @ np.asarray(W_DKV, dtype=float).T
+    y = ORIG["apply_rope"](x @ np.asarray(W_KR, dtype=float).T, pos, base)
+    return c, y.reshape(x.shape[0], n_heads, -1)
+
+
+def _quantize_key_twice_scaled(c, k_r):
+    codes, s, krs = ORIG["quantize_latent_fp8"](c, k_r)
+    return codes, s, ORIG["round_bf16"](np.asarray(krs) / s[..., None])
+
+
 MUTATIONS = [
     ("apply_rope", _rope_wrong_direction, lambda: pins.check_bruteforce(1, **TINY)),
     ("apply_rope", _rope_wrong_direction, lambda: pins.check_rope_properties(16)),
@@ -85,6 +142,15 @@ MUTATIONS = [
     ("output_project", _output_untransposed, lambda: pins.check_bruteforce(1, **TINY)),
     ("project_query", _query_without_rope, lambda: pins.check_bruteforce(1, **TINY)),
     ("compress", _compress_unrotated, lambda: pins.check_bruteforce(1, **TINY)),
+    ("attend_explicit_at", _prefill_window_off_by_one,
+     lambda: pins.check_prefill_rows(6, d_model=40, H=3, qk_nope=7, d_rope=4, v_head=9, d_c=11, L=9, pos=list(range(9)))),
+    ("attend_explicit_at", _prefill_first_head_key, lambda: pins.check_per_head_rope()),
+    ("round_e4m3", _e4m3_ties_away, lambda: pins.check_fp8_format()),
+    ("round_e4m3", _e4m3_no_subnormal_clamp, lambda: pins.check_fp8_format()),
+    ("e4m3_value", _e4m3_value_bias8, lambda: pins.check_fp8_format()),
+    ("fp8_token_scale", _scale_floor, lambda: pins.check_fp8_format()),
+    ("compress_per_head_rope", _per_head_rope_flat, lambda: pins.check_per_head_rope()),
+    ("quantize_latent_fp8", _quantize_key_twice_scaled, lambda: pins.check_fp8_format()),
 ]
 
 
