@@ -122,7 +122,10 @@ typedef struct {
  * block_size * (d_c + 2 d_rope + 4) bytes, element-major per part:
  *   codes  [d_c][block_size] bytes at block offset 0,
  *   k_R/s  [d_rope][block_size] bf16 at block offset d_c * block_size,
- *   s      [block_size] fp32 at block offset (d_c + 2 d_rope) * block_size. */
+ *   s      [block_size] fp32 at block offset (d_c + 2 d_rope) * block_size.
+ * The reduced-precision cache takes block_size 64, d_c a multiple of 64 and
+ * d_rope <= 64; for other shapes every call returns MLA_ERR_UNSUPPORTED and
+ * the size queries return 0. */
 typedef struct {
   void* pool;                   /* device */
   int num_blocks;

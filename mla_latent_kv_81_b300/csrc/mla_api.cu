@@ -88,6 +88,9 @@ mla_status check_cfg(const mla_config* c) {
   if (c->dtype != MLA_F32 && c->dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
   if (c->cache_fp8 != 0 && c->cache_fp8 != 1) return MLA_ERR_INVALID_ARG;
   if (c->cache_fp8 && c->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  // the reduced-precision format's kernels: 64-token blocks, latent in 64-column groups, one warp lane
+  // per positional pair
+  if (c->cache_fp8 && (c->block_size != 64 || c->d_c % 64 || c->d_rope > 64)) return MLA_ERR_UNSUPPORTED;
   if (c->rope_per_head != 0 && c->rope_per_head != 1) return MLA_ERR_INVALID_ARG;
   if (c->rope_per_head && (c->dtype != MLA_BF16 || c->cache_fp8)) return MLA_ERR_UNSUPPORTED;
   if (c->d_rope % 2) return MLA_ERR_UNSUPPORTED;

@@ -109,6 +109,29 @@ def test_bf16_shapes_outside_the_tensor_core_kernels_are_refused_on_the_host():
     assert M.mla_decode_workspace_bytes(M.make_config(dims, "f32"), 2, 1, 4) >= 256
 
 
+def test_reduced_precision_shapes_outside_its_kernels_are_refused_on_the_host():
+    """The reduced-precision cache takes 64-token blocks, a latent in 64-column groups and at most 64
+    positional columns: other shapes get MLA_ERR_UNSUPPORTED from every entry point and zero sizes."""
+    lib, byref = M.lib, ctypes.byref
+    UNS = 2
+    rope = M.mla_rope_table(0x1000, 16)
+    cache = M.mla_paged_cache(0x2000, 4, 0x3000, 2, 2)
+    ok = M.make_config(I.DSV2, "bf16", cache_fp8=True)
+    assert M.mla_cache_bytes_per_token(ok) == 512 + 2 * 64 + 4
+    assert M.mla_compress_workspace_bytes(ok, 2) > 256
+    for dims, bs in [(I.Dims(d_model=5120, n_heads=128, qk_nope=128, d_rope=128, v_head=128, d_c=512), 64),
+                     (I.DSV2, 32)]:
+        cfg = M.make_config(dims, "bf16", cache_fp8=True)
+        cfg.block_size = bs
+        assert M.mla_cache_bytes_per_token(cfg) == 0
+        assert M.mla_compress_workspace_bytes(cfg, 2) == 0
+        assert M.mla_decode_workspace_bytes(cfg, 2, 1, 4) == 0
+        assert lib.mla_compress_append(byref(cfg), _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), byref(rope),
+                                       byref(cache), 2, _fake(6), 1 << 30, None) == UNS
+        assert lib.mla_decode_attention(byref(cfg), _fake(1), byref(cache), _fake(2), 2, 1, _fake(3), None,
+                                        _fake(4), 1 << 30, None) == UNS
+
+
 def test_wait_timeout_selftest_rejects_long_limits_on_the_host():
     """The failure-detection self-check only accepts short limits (at most ~0.1 s of SM cycles) and a
     workspace holding the status header."""
