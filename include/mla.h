@@ -260,8 +260,9 @@ mla_status mla_project_query(const mla_config* cfg, const void* x, const void* W
                              void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /* Workspace bytes mla_prefill_attention needs for a sequence of kv_len cached
- * tokens: the 256-byte header, the sequence's latent rows token-major
- * (kv_len * (d_c + d_rope) bf16) and its rebuilt keys and values
+ * tokens: the 256-byte header, the sequence's cache rows gathered in 64-element
+ * column chunks (kv_len * row bf16, row = d_c + d_rope, or d_c + n_heads * d_rope
+ * with per-head keys) and its rebuilt keys and values
  * (kv_len * n_heads * (qk_nope + v_head) bf16, 64 KB per token at the
  * DeepSeek-V2 shape). */
 size_t mla_prefill_workspace_bytes(const mla_config* cfg, int kv_len);
@@ -282,8 +283,8 @@ size_t mla_prefill_workspace_bytes(const mla_config* cfg, int kv_len);
  *   lse    optional device fp32 [T][n_heads] (natural log of the softmax
  *          normaliser of the scaled scores), or NULL
  * 1 <= T <= kv_len.  Block-table entries outside the pool read as zero rows
- * and are flagged.  With cache_fp8 the gather expands the rows to bf16.  Three launches: the latent gather, the K/V GEMM, the
- * attention kernel. */
+ * and are flagged.  With cache_fp8 the gather expands the rows to bf16.
+ * Three launches: the latent gather, the K/V GEMM, the attention kernel. */
 mla_status mla_prefill_attention(const mla_config* cfg, const void* q, const mla_paged_cache* cache, int seq,
                                  int kv_len, int T, const void* W_UK, const void* W_UV, void* o, float* lse,
                                  void* workspace, size_t workspace_bytes, mla_stream_t stream);
