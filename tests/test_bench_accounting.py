@@ -45,6 +45,35 @@ def test_causal_queries_count_only_visible_tokens():
     assert alg["latent_bytes"] == (12 + 2) * 1152
 
 
+def test_reduced_precision_cache_counts_its_own_row_bytes():
+    b = _bench()
+    p = I.make_problem(I.WORKLOADS["dsv2_b64_ctx8192_fp8"], with_weights=False)
+    alg = b.decode_algorithmic(p)
+    # 512 E4M3 codes + 64 bf16 keys (128 B) + one fp32 scale = 644 B per cached token
+    assert alg["latent_bytes"] == 64 * 8192 * 644 == 337_641_472
+    # queries, outputs and the work per visible token are those of the bf16 cache
+    assert alg["bytes"] == 337_641_472 + 64 * 128 * 1152 + 64 * 128 * 1024 + 64 * 128 * 4
+    assert alg["flops"] == 146_028_888_064
+
+
+def test_prefill_work_of_a_4096_token_prompt():
+    b = _bench()
+    alg = b.prefill_algorithmic(I.PREFILL_CASES["prefill_dsv2_L4096_T4096"])
+    # query j of a whole-prompt prefill sees j + 1 tokens: 4096 * 4097 / 2 (query, key) pairs
+    assert alg["pairs"] == 8_390_656
+    # keys and values rebuilt for every token and head (2 * 512 * (128 + 128) FLOP), then per pair and
+    # head 2 * (128 + 64) for the score and 2 * 128 for P V
+    rebuild = 2 * 4096 * 512 * 128 * 256
+    attend = 2 * 8_390_656 * 128 * 320
+    assert rebuild == 137_438_953_472 and attend == 687_362_539_520
+    assert alg["flops"] == rebuild + attend
+    # bytes: the 4096 cache rows, W_UK and W_UV, the queries and the outputs, all bf16
+    assert alg["bytes"] == 2 * (4096 * 576 + 128 * 256 * 512 + 4096 * 128 * 192 + 4096 * 128 * 128)
+    # per-head positional keys widen each gathered row to 512 + 128 * 64 elements
+    rh = b.prefill_algorithmic(I.PREFILL_CASES["prefill_dsv2_L4096_T4096_rh"])
+    assert rh["bytes"] - alg["bytes"] == 2 * 4096 * 127 * 64
+
+
 def test_recorded_traffic_is_dropped_when_the_sources_change(tmp_path, monkeypatch):
     b = _bench()
     rec = {"workload": "dsv2_b64_ctx8192", "source_sha": b.decode_source_hash(), "dram_bytes_per_launch": 123}
